@@ -1,0 +1,509 @@
+"""Benchmark of the paged-KV attention step (store -> extend -> decode) on GB300.
+
+One step is one pass of the whole hot path over one batch of synthetic
+input: msgl_store_kv writes the step's new K/V rows into the pool,
+msgl_attn_extend runs the chunked prefill, msgl_attn_decode runs the decode
+batch (split chunks + LSE merge).  Inputs are seeded and resident in HBM
+before the timed region.  The headline workload is the Qwen3-32B mixed step
+(64 q heads / 8 kv heads / head_dim 128, page size 64): an 8192-token
+prefill batch (8 requests x 1024 tokens over a shared 2048-token cached
+prefix) plus a 64-request decode batch with lengths 1024-8192.
+
+Printed (rank 0, one JSON line): ``value`` = decode attention KV GB/s
+(algorithmic K+V bytes of every request read once / device time of the
+decode call), ``extend`` = extend TFLOP/s (4*D*Hq per causally valid pair /
+device time of the extend call), both from CUDA events on the launching
+stream over exactly ``--steps`` steps after ``--warmup`` steps, plus the
+roofline of the dominant kernel, the CPU oracle baseline, an end-to-end
+figure through host buffers, and the SM clocks sampled during the run.
+
+``--impl reference`` times the fp64 CPU oracle on the same workload (a
+bounded sample of each step) as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode attn KV GB/s (% HBM peak); extend attn TFLOP/s (% bf16 TC peak)"
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="approximate CPU seconds for the oracle sample")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------- helpers
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "paged_kv_attention_24_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "decode": ["decode.cu", "rows_kernel.cuh", "common.cuh"],
+    "extend": ["extend.cu", "rows_kernel.cuh", "common.cuh"],
+    "store": ["store_kv.cu", "common.cuh"],
+}
+
+
+def recorded_traffic(kind, workload):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current source."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    sha = kernel_source_sha(KERNEL_SOURCES[kind])
+    with open(p) as f:
+        for line in f:
+            if line.startswith("#") or "=" not in line:
+                continue
+            kv = dict(x.split("=", 1) for x in line.split() if "=" in x)
+            if kv.get("kind") == kind and kv.get("workload") == workload and kv.get("src_sha") == sha:
+                try:
+                    return float(kv["dram_bytes_per_launch"])
+                except (KeyError, ValueError):
+                    return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        loaded = [x for x in sm if mx and x > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return ws, rank, local
+
+
+# --------------------------------------------------------- oracle timing
+
+def oracle_sample(w, cpu_seconds, n_threads):
+    """Time the fp64 oracle on a bounded sample of the step; returns a dict of rates."""
+    import numpy as np
+    import oracle
+    res = {"cores": n_threads, "kind": "oracle"}
+    kp, vp = w.k_pool.cpu(), w.v_pool.cpu()
+    budget = cpu_seconds / 2
+    # decode: whole requests (every q head), growing until the time budget is used
+    dec_bytes = dec_time = 0.0
+    dec_reqs = 0
+    if w.decode is not None:
+        d = w.decode
+        q, pt, seq = d.q.cpu(), d.page_table.cpu(), d.seq_lens.cpu().numpy()
+        b = 0
+        while b < d.num_reqs and dec_time < budget:
+            n = min(d.num_reqs - b, max(1, n_threads // 4))
+            rows = np.arange(b, b + n, dtype=np.int32)
+            req = np.repeat(rows, w.hq)
+            head = np.tile(np.arange(w.hq, dtype=np.int32), n)
+            pos = seq[req] - 1
+            t0 = time.perf_counter()
+            oracle.attention_items(q, kp, vp, w.page_size, pt, w.scale, req, req, pos, head,
+                                   n_threads=n_threads)
+            dec_time += time.perf_counter() - t0
+            dec_bytes += float(seq[b:b + n].sum()) * w.hkv * w.d * 4
+            dec_reqs += n
+            b += n
+    ext_flops = ext_time = 0.0
+    ext_rows = 0
+    if w.extend is not None:
+        e = w.extend
+        q, pt = e.q.cpu(), e.page_table.cpu()
+        cu, pre = e.cu_ext.cpu().numpy(), e.prefix_lens.cpu().numpy()
+        rng = np.random.default_rng(0)
+        while ext_time < budget and ext_rows < e.total_tokens:
+            toks = rng.integers(0, e.total_tokens, size=max(1, n_threads // 2)).astype(np.int32)
+            r_of = np.searchsorted(cu, toks, side="right") - 1
+            pos = pre[r_of] + toks - cu[r_of]
+            req = np.repeat(r_of, w.hq).astype(np.int32)
+            row = np.repeat(toks, w.hq).astype(np.int32)
+            pp = np.repeat(pos, w.hq).astype(np.int32)
+            head = np.tile(np.arange(w.hq, dtype=np.int32), len(toks))
+            t0 = time.perf_counter()
+            oracle.attention_items(q, kp, vp, w.page_size, pt, w.scale, req, row, pp, head,
+                                   n_threads=n_threads)
+            ext_time += time.perf_counter() - t0
+            ext_flops += float((pos + 1).sum()) * 4 * w.d * w.hq
+            ext_rows += len(toks)
+    res["decode_gbs"] = dec_bytes / dec_time / 1e9 if dec_time else None
+    res["extend_tflops"] = ext_flops / ext_time / 1e12 if ext_time else None
+    res["sample"] = (f"{dec_reqs} decode requests x {w.hq} heads ({dec_time:.1f} s); "
+                     f"{ext_rows} random extend rows x {w.hq} heads ({ext_time:.1f} s)")
+    res["seconds"] = dec_time + ext_time
+    return res
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    ws, rank, local = dist_info()
+    if rank != 0:
+        return 0
+    import torch  # noqa: F401
+    from paged_kv_attention_24_gb300 import workloads as W
+    from paged_kv_attention_24_gb300 import accounting as A
+    import oracle
+    w = W.config(args.config, device="cpu")
+    threads = oracle.default_threads()
+    per_step = max(1.0, 90.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(w, min(per_step, 2.0), threads)
+    vals, tf, secs = [], [], 0.0
+    last = None
+    for _ in range(args.steps):
+        r = oracle_sample(w, per_step, threads)
+        secs += r["seconds"]
+        if r["decode_gbs"] is not None:
+            vals.append(r["decode_gbs"])
+        if r["extend_tflops"] is not None:
+            tf.append(r["extend_tflops"])
+        last = r
+    value = statistics.mean(vals) if vals else None
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * secs / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": W.CONFIG_NAMES[args.config], "config_id": args.config,
+                   "decode_kv_bytes_per_step": A.decode_kv_bytes(w),
+                   "extend_flop_per_step": A.extend_flops(w)},
+        "extend": {"value": statistics.mean(tf) if tf else None, "unit": "TFLOP/s"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": "each step: " + (last["sample"] if last else "")},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import torch
+    ws, rank, local = dist_info()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    from paged_kv_attention_24_gb300 import build as cuda_build
+    cuda_build.build()
+    from paged_kv_attention_24_gb300 import ops
+    from paged_kv_attention_24_gb300 import workloads as W
+    from paged_kv_attention_24_gb300 import accounting as A
+
+    w = W.config(args.config, device=dev, seed=1000 + args.config + 7 * rank)
+    pool = ops.KVPool(w.k_pool, w.v_pool, w.page_size)
+    k_new, v_new, loc = w.new_tokens()
+    e, d = w.extend, w.decode
+    stream = torch.cuda.current_stream()
+    o_e = torch.empty_like(e.q) if e else None
+    l_e = torch.empty(e.q.shape[:2], dtype=torch.float32, device=dev) if e else None
+    o_d = torch.empty_like(d.q) if d else None
+    l_d = torch.empty(d.q.shape[:2], dtype=torch.float32, device=dev) if d else None
+    ws_d = ws_e = None
+    if d is not None:
+        n = ops.decode_workspace_size(d.num_reqs, w.hq, w.hkv, d.max_seq_len)
+        ws_d = torch.empty(n, dtype=torch.uint8, device=dev) if n else None
+    if e is not None:
+        n = ops.extend_workspace_size(e.num_reqs, e.total_tokens, w.hq, w.hkv, e.max_seq_len)
+        ws_e = torch.empty(n, dtype=torch.uint8, device=dev) if n else None
+    status = ops.new_status(dev)
+    launches_per_step = (1 if loc.numel() else 0) + (1 if e is not None else 0) + \
+        ((2 if ws_d is not None else 1) if d is not None else 0)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        ops.store_kv(pool, k_new, v_new, loc, status=status)
+        if ev:
+            ev[1].record(stream)
+        if e is not None:
+            ops.attn_extend(pool, e.q, e.page_table, e.prefix_lens, e.ext_lens, e.cu_ext,
+                            e.max_ext_len, e.max_seq_len, w.scale, positions=e.positions,
+                            out=o_e, lse=l_e, workspace=ws_e, status=status)
+        if ev:
+            ev[2].record(stream)
+        if d is not None:
+            ops.attn_decode(pool, d.q, d.page_table, d.seq_lens, d.max_seq_len, w.scale,
+                            out=o_d, lse=l_d, workspace=ws_d, status=status)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert ops.read_status(status) == 0, "device status set during warm-up"
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    store_ms = [ev[0].elapsed_time(ev[1]) for ev in evs]
+    ext_ms = [ev[1].elapsed_time(ev[2]) for ev in evs]
+    dec_ms = [ev[2].elapsed_time(ev[3]) for ev in evs]
+    mean = statistics.mean
+    dec_bytes, ext_flops, st_bytes = A.decode_kv_bytes(w), A.extend_flops(w), A.store_bytes(w)
+
+    if ws > 1:
+        t = torch.tensor([total_ms, mean(dec_ms), mean(ext_ms)], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms, dec_avg, ext_avg = t.tolist()
+    else:
+        dec_avg, ext_avg = mean(dec_ms), mean(ext_ms)
+    st_avg = mean(store_ms)
+    peaks = load_peaks()
+    dec_gbs = ws * dec_bytes / (dec_avg * 1e-3) / 1e9 if d is not None else None
+    ext_tf = ws * ext_flops / (ext_avg * 1e-3) / 1e12 if e is not None else None
+    st_gbs = st_bytes / (st_avg * 1e-3) / 1e9 if st_avg > 0 else None
+
+    per_gpu_dec = dec_bytes / (dec_avg * 1e-3) / 1e9 if d is not None else None
+    per_gpu_ext = ext_flops / (ext_avg * 1e-3) / 1e12 if e is not None else None
+    rooflines = {}
+    if d is not None:
+        rooflines["decode"] = {"bound": "hbm", "achieved": per_gpu_dec, "peak": peaks["hbm_gbs"],
+                               "unit": "GB/s", "frac": per_gpu_dec / peaks["hbm_gbs"],
+                               "traffic": recorded_traffic("decode", W.CONFIG_NAMES[args.config]),
+                               "us_per_launch": dec_avg * 1e3}
+    if e is not None:
+        pk = peaks["bf16_tflops_sustained"]
+        rooflines["extend"] = {"bound": "tensor", "achieved": per_gpu_ext, "peak": pk,
+                               "unit": "TFLOP/s", "frac": per_gpu_ext / pk,
+                               "traffic": recorded_traffic("extend", W.CONFIG_NAMES[args.config]),
+                               "us_per_launch": ext_avg * 1e3}
+    if st_gbs:
+        rooflines["store"] = {"bound": "hbm", "achieved": st_gbs, "peak": peaks["hbm_gbs"],
+                              "unit": "GB/s", "frac": st_gbs / peaks["hbm_gbs"],
+                              "traffic": recorded_traffic("store", W.CONFIG_NAMES[args.config]),
+                              "us_per_launch": st_avg * 1e3}
+    dominant = max(rooflines, key=lambda k: rooflines[k]["us_per_launch"])
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(args, w, pool, k_new, v_new, loc, dev, dec_bytes, ext_flops)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        wc = w.to("cpu")
+        r = oracle_sample(wc, args.cpu_seconds, oracle.default_threads())
+        cpu = {"value": r["decode_gbs"], "unit": "GB/s", "cores": r["cores"], "kind": "oracle",
+               "sample": r["sample"], "extend_tflops": r["extend_tflops"]}
+
+    if rank != 0:
+        return 0
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": dec_gbs, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": W.CONFIG_NAMES[args.config], "config_id": args.config,
+                   "hq": w.hq, "hkv": w.hkv, "head_dim": w.d, "page_size": w.page_size,
+                   "decode_batch": d.num_reqs if d else 0,
+                   "extend_tokens": e.total_tokens if e else 0,
+                   "decode_kv_bytes_per_step": dec_bytes, "extend_flop_per_step": ext_flops,
+                   "l2": "inputs larger than L2 (decode KV %.2f GB per step), no flush" % (dec_bytes / 1e9),
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "extend": {"value": ext_tf, "unit": "TFLOP/s",
+                   "frac": (per_gpu_ext / peaks["bf16_tflops_sustained"]) if e else None},
+        "store": {"value": st_gbs, "unit": "GB/s"},
+        "roofline": dict(rooflines[dominant], kernel=dominant),
+        "rooflines": rooflines,
+        "peaks": peaks,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def measure_e2e(args, w, pool, k_new, v_new, loc, dev, dec_bytes, ext_flops):
+    """Same step through the public API with host buffers: H2D inputs, kernels, D2H outputs."""
+    import torch
+    from paged_kv_attention_24_gb300 import ops
+    e, d = w.extend, w.decode
+    stream = torch.cuda.current_stream()
+
+    def pinned(t):
+        return t.detach().to("cpu").pin_memory()
+
+    host_in = {"k_new": pinned(k_new), "v_new": pinned(v_new), "loc": pinned(loc)}
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    if e is not None:
+        for name in ("q", "page_table", "prefix_lens", "ext_lens", "cu_ext", "positions"):
+            host_in["e_" + name] = pinned(getattr(e, name))
+            dev_in["e_" + name] = torch.empty_like(host_in["e_" + name], device=dev)
+    if d is not None:
+        for name in ("q", "page_table", "seq_lens"):
+            host_in["d_" + name] = pinned(getattr(d, name))
+            dev_in["d_" + name] = torch.empty_like(host_in["d_" + name], device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    outs = {}
+    if e is not None:
+        outs["e_o"] = torch.empty_like(e.q).cpu().pin_memory()
+        outs["e_l"] = torch.empty(e.q.shape[:2], dtype=torch.float32).pin_memory()
+    if d is not None:
+        outs["d_o"] = torch.empty_like(d.q).cpu().pin_memory()
+        outs["d_l"] = torch.empty(d.q.shape[:2], dtype=torch.float32).pin_memory()
+    d2h = sum(t.numel() * t.element_size() for t in outs.values())
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        for k in ("k_new", "v_new", "loc"):
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        ops.store_kv(pool, dev_in["k_new"], dev_in["v_new"], dev_in["loc"])
+        if ev:
+            ev[1].record(stream)
+        if e is not None:
+            for name in ("q", "page_table", "prefix_lens", "ext_lens", "cu_ext", "positions"):
+                dev_in["e_" + name].copy_(host_in["e_" + name], non_blocking=True)
+            o, l = ops.attn_extend(pool, dev_in["e_q"], dev_in["e_page_table"], dev_in["e_prefix_lens"],
+                                   dev_in["e_ext_lens"], dev_in["e_cu_ext"], e.max_ext_len,
+                                   e.max_seq_len, w.scale, positions=dev_in["e_positions"])
+            outs["e_o"].copy_(o, non_blocking=True)
+            outs["e_l"].copy_(l, non_blocking=True)
+        if ev:
+            ev[2].record(stream)
+        if d is not None:
+            for name in ("q", "page_table", "seq_lens"):
+                dev_in["d_" + name].copy_(host_in["d_" + name], non_blocking=True)
+            o, l = ops.attn_decode(pool, dev_in["d_q"], dev_in["d_page_table"], dev_in["d_seq_lens"],
+                                   d.max_seq_len, w.scale)
+            outs["d_o"].copy_(o, non_blocking=True)
+            outs["d_l"].copy_(l, non_blocking=True)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        step(evs[i])
+    torch.cuda.synchronize()
+    ext_ms = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs)
+    dec_ms = statistics.mean(ev[2].elapsed_time(ev[3]) for ev in evs)
+    step_ms = statistics.mean(ev[0].elapsed_time(ev[3]) for ev in evs)
+    return {"value": dec_bytes / (dec_ms * 1e-3) / 1e9 if d is not None else None, "unit": "GB/s",
+            "extend_tflops": ext_flops / (ext_ms * 1e-3) / 1e12 if e is not None else None,
+            "ms_per_step": step_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "note": "decode and extend calls each timed with their own input H2D and output D2H copies"}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,205 @@
+/*
+ * libmsgl_attn — paged-KV grouped-query attention for GB300 (sm_103a).
+ *
+ * The attention step a Mini-SGLang-style serving engine runs every forward:
+ * new K/V rows are scattered into a unified, paged KV pool, then prefill
+ * chunks ("extend") and single-token decode rows attend over each request's
+ * pages.  The pages describing the engine define the pieces this ABI takes:
+ *
+ *   - one unified KV pool, allocated in pages of a configurable size
+ *     ("Mini-SGLang 实战指南", §6.2 "Page Size"; §6.5 "Radix Cache";
+ *     "不懂SGLang？从miniSGLang开始", §1.2 "调度引擎", item 3);
+ *   - attention reads the pool's history plus the newly computed K/V, and
+ *     locates each request's data through the page table and positions
+ *     ("不懂SGLang？从miniSGLang开始", §1.3 "前向运算", items 1 and 3);
+ *   - prefill runs in chunks over a cached (radix-shared) prefix
+ *     ("Mini-SGLang 实战指南", §6.1 "Chunked Prefill", §6.5);
+ *   - prefill and decode are separate attention calls
+ *     ("Mini-SGLang 实战指南", §6.3).
+ *
+ * Definitions used by every call (the pages fix no formula; this is the
+ * plain reading of causal softmax attention with grouped heads):
+ *   G        = num_q_heads / num_kv_heads; q head h reads kv head h / G
+ *   slot(j)  = page_table[b][j / page_size] * page_size + j % page_size
+ *   a query row at absolute position p attends keys j = 0..p:
+ *   s_j = scale * <q, K[slot(j)][h/G]>,  o = sum_j softmax(s)_j V[slot(j)][h/G],
+ *   lse = ln(sum_j exp(s_j))   (natural log, fp32)
+ *
+ * Conventions
+ *   - Every pointer named "device" is CUDA device memory owned by the
+ *     caller; the library allocates nothing, keeps no state between calls
+ *     and never frees caller memory.  All calls are asynchronous on
+ *     `stream` (NULL = the legacy default stream) except msgl_read_status.
+ *   - bf16 tensors are row-major, contiguous, 16-byte aligned.
+ *   - Host-side validation failures return before anything is launched.
+ *   - Device-side index errors never trap: the kernel ORs a bit into the
+ *     caller's status word (when `status` is non-NULL), skips the bad
+ *     access and writes that output row as o = 0, lse = -inf.
+ *   - Waits inside kernels are bounded; a wait that gives up sets
+ *     MSGL_DEVERR_TIMEOUT and the kernel returns.
+ */
+#ifndef MSGL_ATTN_H
+#define MSGL_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MSGL_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define MSGL_API __attribute__((visibility("default")))
+#else
+#define MSGL_API
+#endif
+
+/* A cudaStream_t (the runtime and driver stream handle types are the same pointer). */
+typedef struct CUstream_st *msgl_stream_t;
+
+typedef enum msgl_status {
+    MSGL_OK = 0,
+    MSGL_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or scalar */
+    MSGL_ERR_UNSUPPORTED = 2,   /* valid but not implemented (head_dim != 128, ...) */
+    MSGL_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed (launch, copy) */
+    MSGL_ERR_OUT_OF_RANGE = 4,  /* reported by msgl_read_status: device index error */
+    MSGL_ERR_TIMEOUT = 5,       /* reported by msgl_read_status: a bounded wait gave up */
+    MSGL_ERR_WORKSPACE = 6      /* workspace missing or smaller than the size query */
+} msgl_status;
+
+/* Bits of the device status word (uint32, caller-owned device memory). */
+#define MSGL_DEVERR_SLOT_RANGE 0x1u  /* out_loc entry outside [0, num_slots) */
+#define MSGL_DEVERR_PAGE_RANGE 0x2u  /* page index >= width, or page id outside the pool */
+#define MSGL_DEVERR_LENGTH 0x4u      /* decode seq_len < 1, or lengths inconsistent with cu_ext */
+#define MSGL_DEVERR_POSITION 0x8u    /* positions[t] != prefix_len + i for chunk row i */
+#define MSGL_DEVERR_TIMEOUT 0x10u    /* a bounded in-kernel wait gave up */
+
+/*
+ * The unified KV pool of one layer.  k_pool and v_pool are device bf16
+ * [num_slots, num_kv_heads, head_dim], slot-major (the row of one slot is
+ * num_kv_heads*head_dim contiguous elements).  num_slots must be a multiple
+ * of page_size; page_size is a power of two in [1, 256]; head_dim must be 128.
+ */
+typedef struct msgl_kv_pool {
+    void *k_pool;
+    void *v_pool;
+    int64_t num_slots;
+    int32_t page_size;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+} msgl_kv_pool;
+
+/*
+ * Per-request page table: device int32 [num_reqs, stride]; row b lists the
+ * page ids of request b in sequence order.  Only the first `width` entries
+ * of a row may be read; a key whose page index reaches `width`, or whose
+ * page id lies outside [0, num_slots/page_size), is a device index error.
+ */
+typedef struct msgl_page_table {
+    const int32_t *page_ids;
+    int32_t stride;
+    int32_t width;
+} msgl_page_table;
+
+/*
+ * Store step: write the new K/V rows of this forward into the pool
+ * ("不懂SGLang？从miniSGLang开始", §1.3 item 1: the KV an attention call
+ * reads is the pool's history plus the newly computed KV; every request
+ * allocates from the one pool, §1.2 item 3).
+ *
+ *   k, v     device bf16 [n_tokens, num_kv_heads, head_dim]
+ *   out_loc  device int32 [n_tokens]; row t goes to slot out_loc[t]
+ *   status   device uint32 or NULL
+ * Pool rows not named in out_loc are untouched.  Duplicate slots in out_loc
+ * are undefined (one of the rows wins).  An out-of-range slot sets
+ * MSGL_DEVERR_SLOT_RANGE and that row is skipped.  The copy is bit-exact.
+ */
+MSGL_API msgl_status msgl_store_kv(const msgl_kv_pool *pool, const void *k, const void *v,
+                          const int32_t *out_loc, int32_t n_tokens, uint32_t *status,
+                          msgl_stream_t stream);
+
+/*
+ * Extend (chunked prefill) step: request b has prefix_lens[b] tokens already
+ * cached in its pages (a radix-cache hit or earlier chunks) and ext_lens[b]
+ * new tokens whose K/V have already been stored in the pool by
+ * msgl_store_kv.  Chunk row i of request b sits at absolute position
+ * prefix_lens[b] + i and attends keys 0..prefix_lens[b]+i
+ * ("Mini-SGLang 实战指南", §6.1 "Chunked Prefill", §6.5 "Radix Cache";
+ * "不懂SGLang？从miniSGLang开始", §1.3).
+ *
+ *   q            device bf16 [total_tokens, num_q_heads, head_dim],
+ *                request-major: request b owns rows cu_ext[b]..cu_ext[b+1]-1
+ *   prefix_lens, ext_lens   device int32 [num_reqs]
+ *   cu_ext       device int32 [num_reqs+1], cu_ext[0] = 0, prefix sums of ext_lens
+ *   positions    device int32 [total_tokens] or NULL; when given, each row's
+ *                entry must equal prefix_lens[b] + i (checked, else
+ *                MSGL_DEVERR_POSITION; the mask always comes from the lengths)
+ *   max_ext_len, max_seq_len   host upper bounds of ext_lens[b] and
+ *                prefix_lens[b]+ext_lens[b]; they size the grid (a value
+ *                that is too small is a device length error, never a wild read)
+ *   scale        softmax scale (> 0, finite), normally 1/sqrt(head_dim)
+ *   o            device bf16 [total_tokens, num_q_heads, head_dim] (output)
+ *   lse          device fp32 [total_tokens, num_q_heads] (output), natural log
+ *   workspace    device scratch of msgl_extend_workspace_size() bytes (may be
+ *                NULL when that size is 0)
+ */
+MSGL_API size_t msgl_extend_workspace_size(int32_t num_reqs, int32_t total_tokens, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t max_seq_len);
+
+MSGL_API msgl_status msgl_attn_extend(const msgl_kv_pool *pool, const msgl_page_table *pages,
+                             const void *q, int32_t num_q_heads, const int32_t *prefix_lens,
+                             const int32_t *ext_lens, const int32_t *cu_ext,
+                             const int32_t *positions, int32_t num_reqs, int32_t total_tokens,
+                             int32_t max_ext_len, int32_t max_seq_len, float scale, void *o,
+                             float *lse, void *workspace, size_t workspace_bytes,
+                             uint32_t *status, msgl_stream_t stream);
+
+/*
+ * Decode step: one query row per request at position seq_lens[b]-1; it
+ * attends all seq_lens[b] keys, the current token's included (stored by
+ * msgl_store_kv first) ("Mini-SGLang 实战指南", §6.3 and §6.4: the decode
+ * kernel is separate from prefill and is replayed under CUDA graphs, so the
+ * grid depends only on the host scalars num_reqs and max_seq_len).
+ * The keys are split into chunks processed in parallel, and the partial
+ * results are merged by their log-sum-exp in a second kernel.
+ *
+ *   q          device bf16 [num_reqs, num_q_heads, head_dim]
+ *   seq_lens   device int32 [num_reqs], each >= 1 and <= max_seq_len
+ *   o, lse     device bf16 [num_reqs, num_q_heads, head_dim], fp32 [num_reqs, num_q_heads]
+ *   workspace  device scratch of at least msgl_decode_workspace_size() bytes,
+ *              256-byte aligned; it holds the split partials (fp32) and is
+ *              fully rewritten by every call
+ */
+MSGL_API size_t msgl_decode_workspace_size(int32_t num_reqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_seq_len);
+
+MSGL_API msgl_status msgl_attn_decode(const msgl_kv_pool *pool, const msgl_page_table *pages,
+                             const void *q, int32_t num_q_heads, const int32_t *seq_lens,
+                             int32_t num_reqs, int32_t max_seq_len, float scale, void *o,
+                             float *lse, void *workspace, size_t workspace_bytes,
+                             uint32_t *status, msgl_stream_t stream);
+
+/*
+ * Synchronises `stream`, reads the device status word into *flags (may be
+ * NULL) and maps it to a status: MSGL_OK when it is zero, MSGL_ERR_TIMEOUT
+ * when the timeout bit is set, else MSGL_ERR_OUT_OF_RANGE.  For tests and
+ * debugging; not meant for the hot path.
+ */
+MSGL_API msgl_status msgl_read_status(const uint32_t *status, uint32_t *flags, msgl_stream_t stream);
+
+/* Static description of a status code. */
+MSGL_API const char *msgl_status_string(msgl_status s);
+
+/* Thread-local text of the last failure in this thread (empty if none). */
+MSGL_API const char *msgl_last_error(void);
+
+/* MSGL_ABI_VERSION of the built library. */
+MSGL_API int32_t msgl_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSGL_ATTN_H */

@@ -1,0 +1,59 @@
+// Launchers shared between the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace msgl {
+
+// ---------------------------------------------------------------- store
+cudaError_t launch_store_kv(const PoolView &pool, __nv_bfloat16 *k_pool, __nv_bfloat16 *v_pool,
+                            const __nv_bfloat16 *k, const __nv_bfloat16 *v,
+                            const int32_t *out_loc, int32_t n_tokens, uint32_t *status,
+                            cudaStream_t stream);
+
+// --------------------------------------------------------------- decode
+struct DecodePlan {
+    int32_t num_splits;   // key chunks per request
+    int32_t chunk;        // keys per chunk (multiple of 64)
+    size_t workspace;     // bytes of split partials
+};
+DecodePlan plan_decode(int32_t num_reqs, int32_t hq, int32_t hkv, int32_t max_seq_len);
+
+struct DecodeArgs {
+    PoolView pool;
+    PageView pages;
+    const __nv_bfloat16 *q;
+    const int32_t *seq_lens;
+    int32_t num_reqs, hq, max_seq_len;
+    float scale;
+    __nv_bfloat16 *o;
+    float *lse;
+    float *part_o;      // [num_reqs, hq, num_splits, 128]
+    float *part_lse;    // [num_reqs, hq, num_splits]
+    uint32_t *status;
+};
+cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream);
+
+// --------------------------------------------------------------- extend
+size_t extend_workspace_bytes(int32_t num_reqs, int32_t total_tokens, int32_t hq, int32_t hkv,
+                              int32_t max_seq_len);
+
+struct ExtendArgs {
+    PoolView pool;
+    PageView pages;
+    const __nv_bfloat16 *q;
+    const int32_t *prefix_lens, *ext_lens, *cu_ext, *positions;
+    int32_t num_reqs, total_tokens, hq, max_ext_len, max_seq_len;
+    float scale;
+    __nv_bfloat16 *o;
+    float *lse;
+    void *workspace;
+    uint32_t *status;
+};
+cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t stream);
+
+}  // namespace msgl

@@ -1,0 +1,152 @@
+"""msgl_attn_extend against the fp64 oracle on the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_attention_24_gb300 import ops
+from paged_kv_attention_24_gb300 import workloads as W
+from tests.parity import assert_lse_close, assert_o_close
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(w, status=None, q=None, prefix=None, ext=None, cu=None, positions=None):
+    e = w.extend
+    pool = ops.KVPool(w.k_pool, w.v_pool, w.page_size)
+    return ops.attn_extend(pool, e.q if q is None else q, e.page_table,
+                           e.prefix_lens if prefix is None else prefix,
+                           e.ext_lens if ext is None else ext, e.cu_ext if cu is None else cu,
+                           e.max_ext_len, e.max_seq_len, w.scale,
+                           positions=e.positions if positions is None else positions, status=status)
+
+
+def run_oracle(w, tokens=None):
+    e = w.extend
+    kp, vp = w.k_pool.cpu(), w.v_pool.cpu()
+    if tokens is None:
+        return oracle.extend(e.q.cpu(), kp, vp, w.page_size, e.page_table.cpu(), e.prefix_lens.cpu(),
+                             e.ext_lens.cpu(), w.scale)
+    cu = e.cu_ext.cpu().numpy()
+    pre = e.prefix_lens.cpu().numpy()
+    tokens = np.asarray(tokens, dtype=np.int32)
+    req_of = np.searchsorted(cu, tokens, side="right") - 1
+    pos = pre[req_of] + (tokens - cu[req_of])
+    req = np.repeat(req_of, w.hq).astype(np.int32)
+    row = np.repeat(tokens, w.hq).astype(np.int32)
+    pp = np.repeat(pos, w.hq).astype(np.int32)
+    head = np.tile(np.arange(w.hq, dtype=np.int32), len(tokens))
+    o, lse = oracle.attention_items(e.q.cpu(), kp, vp, w.page_size, e.page_table.cpu(), w.scale,
+                                    req, row, pp, head)
+    return o.reshape(len(tokens), w.hq, w.d), lse.reshape(len(tokens), w.hq)
+
+
+def sample_tokens(w, n_random=96, seed=0):
+    """First/last rows of every request, rows at tile boundaries, and random rows."""
+    e = w.extend
+    cu = e.cu_ext.cpu().numpy()
+    picks = set()
+    for b in range(len(cu) - 1):
+        lo, hi = int(cu[b]), int(cu[b + 1])
+        for t in (lo, lo + 1, hi - 2, hi - 1):
+            if lo <= t < hi:
+                picks.add(t)
+        for k in (16, 25, 64, 128, 256):
+            for t in (lo + k - 1, lo + k):
+                if lo <= t < hi:
+                    picks.add(t)
+    rng = np.random.default_rng(seed)
+    picks.update(rng.integers(0, int(cu[-1]), size=n_random).tolist())
+    return np.array(sorted(picks), dtype=np.int32)
+
+
+def test_extend_config2_full():
+    w = W.config(2, device="cuda", part="extend")
+    status = ops.new_status()
+    o, lse = run_gpu(w, status)
+    assert ops.read_status(status) == 0
+    ref_o, ref_l = run_oracle(w)
+    assert_o_close(o, ref_o, "config 2")
+    assert_lse_close(lse, ref_l, "config 2")
+
+
+@pytest.mark.parametrize("cfg", [4, 5])
+def test_extend_large_configs_sampled(cfg):
+    w = W.config(cfg, device="cuda", part="extend")
+    status = ops.new_status()
+    o, lse = run_gpu(w, status)
+    assert ops.read_status(status) == 0
+    toks = sample_tokens(w, seed=cfg)
+    ref_o, ref_l = run_oracle(w, toks)
+    idx = torch.from_numpy(toks).long().cuda()
+    assert_o_close(o[idx], ref_o, f"config {cfg}")
+    assert_lse_close(lse[idx], ref_l, f"config {cfg}")
+    # every row finite, and every row's LSE at least the log of its key count minus a margin
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("ps", [1, 16, 64, 256])
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (40, 8), (64, 8), (8, 8), (4, 1)])
+def test_extend_ragged_shapes(ps, hq, hkv):
+    pre = [0, 5, 130, 0, 1000, 64, 255]
+    ext = [1, 127, 128, 129, 33, 300, 2]
+    w = W.make_workload("ragged", hq, hkv, 128, ps, seed=ps + hq, extend_prefix_lens=pre,
+                        extend_ext_lens=ext, device="cuda")
+    o, lse = run_gpu(w)
+    ref_o, ref_l = run_oracle(w)
+    assert_o_close(o, ref_o, f"ps={ps} hq={hq}")
+    assert_lse_close(lse, ref_l)
+
+
+def test_extend_shared_prefix_pages():
+    """Requests whose page tables point at the same prefix pages (radix hit)."""
+    w = W.make_workload("shared", 64, 8, 128, 64, seed=9, extend_prefix_lens=[512] * 4,
+                        extend_ext_lens=[200, 64, 1, 333], shared_prefix_len=512, device="cuda")
+    o, lse = run_gpu(w)
+    ref_o, ref_l = run_oracle(w)
+    assert_o_close(o, ref_o)
+    assert_lse_close(lse, ref_l)
+
+
+def test_chunked_equals_unchunked_on_gpu():
+    """A 700-token prefill run as chunks 300 + 250 + 150 matches the single pass (both vs oracle)."""
+    w = W.make_workload("chunks", 16, 8, 128, 16, seed=10, extend_prefix_lens=[0], extend_ext_lens=[700],
+                        device="cuda")
+    o_full, l_full = run_gpu(w)
+    e = w.extend
+    pool = ops.KVPool(w.k_pool, w.v_pool, w.page_size)
+    for lo, hi in ((0, 300), (300, 550), (550, 700)):
+        n = hi - lo
+        o, l = ops.attn_extend(pool, e.q[lo:hi].contiguous(), e.page_table,
+                               torch.tensor([lo], dtype=torch.int32, device="cuda"),
+                               torch.tensor([n], dtype=torch.int32, device="cuda"),
+                               torch.tensor([0, n], dtype=torch.int32, device="cuda"), n, hi, w.scale)
+        assert (o.float() - o_full[lo:hi].float()).abs().max().item() <= 1e-2
+        assert (l - l_full[lo:hi]).abs().max().item() <= 1e-3
+    ref_o, ref_l = run_oracle(w)
+    assert_o_close(o_full, ref_o)
+
+
+def test_decode_equals_last_extend_row():
+    w = W.make_workload("last", 40, 8, 128, 16, seed=11, extend_prefix_lens=[100, 0],
+                        extend_ext_lens=[57, 300], device="cuda")
+    o_e, l_e = run_gpu(w)
+    e = w.extend
+    pool = ops.KVPool(w.k_pool, w.v_pool, w.page_size)
+    last = (e.cu_ext[1:] - 1).long()
+    seq = (e.prefix_lens + e.ext_lens).int()
+    o_d, l_d = ops.attn_decode(pool, e.q[last].contiguous(), e.page_table, seq, int(seq.max()), w.scale)
+    assert (o_d.float() - o_e[last].float()).abs().max().item() <= 1e-2
+    assert (l_d - l_e[last]).abs().max().item() <= 1e-3
+
+
+def test_extend_without_positions():
+    w = W.make_workload("nopos", 16, 8, 128, 1, seed=12, extend_prefix_lens=[3], extend_ext_lens=[40],
+                        device="cuda")
+    e = w.extend
+    pool = ops.KVPool(w.k_pool, w.v_pool, w.page_size)
+    o, lse = ops.attn_extend(pool, e.q, e.page_table, e.prefix_lens, e.ext_lens, e.cu_ext,
+                             e.max_ext_len, e.max_seq_len, w.scale, positions=None)
+    ref_o, ref_l = run_oracle(w)
+    assert_o_close(o, ref_o)
+    assert_lse_close(lse, ref_l)
