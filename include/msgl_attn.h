@@ -182,6 +182,34 @@ MSGL_API msgl_status msgl_attn_decode(const msgl_kv_pool *pool, const msgl_page_
                              uint32_t *status, msgl_stream_t stream);
 
 /*
+ * Decode for callers that cannot allocate device memory.  It has no
+ * counterpart on the pages describing the engine: it is msgl_attn_decode
+ * with its split scratch taken from a fixed array inside the library
+ * instead of a caller workspace.  Meant for callers whose device memory is
+ * all owned by a host pool planned up front, plugin-style interfaces that
+ * receive only input and output pointers, and loops that cannot afford
+ * cudaMalloc's implicit device synchronisation.
+ *
+ * Arguments, layouts, outputs and device status bits are those of
+ * msgl_attn_decode, minus the workspace.  It allocates nothing: the scratch
+ * is a static device array of MSGL_DECODE_NOALLOC_SCRATCH_BYTES that every
+ * GPU loading the library holds until the process exits.  A call whose
+ * msgl_decode_workspace_size() exceeds that size returns
+ * MSGL_ERR_WORKSPACE (msgl_last_error() gives both sizes) without launching.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before capturing any stream.  All calls on a device share the
+ * array, which keeps the last call's contents (no call relies on them);
+ * calls whose kernels overlap on the GPU race on it, so order them.
+ */
+#define MSGL_DECODE_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+MSGL_API msgl_status msgl_attn_decode_noalloc(const msgl_kv_pool *pool, const msgl_page_table *pages,
+                                     const void *q, int32_t num_q_heads, const int32_t *seq_lens,
+                                     int32_t num_reqs, int32_t max_seq_len, float scale, void *o,
+                                     float *lse, uint32_t *status, msgl_stream_t stream);
+
+/*
  * Synchronises `stream`, reads the device status word into *flags (may be
  * NULL) and maps it to a status: MSGL_OK when it is zero, MSGL_ERR_TIMEOUT
  * when the timeout bit is set, else MSGL_ERR_OUT_OF_RANGE.  For tests and

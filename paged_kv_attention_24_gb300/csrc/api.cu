@@ -85,6 +85,11 @@ msgl_status check_scale(float scale) {
 
 }  // namespace
 
+namespace msgl {
+// Lets other translation units of the library set this thread's error text.
+void set_last_error(const char *msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+}  // namespace msgl
+
 extern "C" {
 
 int32_t msgl_abi_version(void) { return MSGL_ABI_VERSION; }

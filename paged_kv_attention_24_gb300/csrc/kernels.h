@@ -56,4 +56,7 @@ struct ExtendArgs {
 };
 cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t stream);
 
+// Sets the text msgl_last_error() returns on this thread.
+void set_last_error(const char *msg);
+
 }  // namespace msgl

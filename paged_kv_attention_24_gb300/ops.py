@@ -61,6 +61,7 @@ SIGNATURES = {
                          ctypes.c_int),
     "msgl_decode_workspace_size": ([I32, I32, I32, I32, I32], SZ),
     "msgl_attn_decode": ([PP, PT, P, I32, P, I32, I32, F32, P, P, P, SZ, P, P], ctypes.c_int),
+    "msgl_attn_decode_noalloc": ([PP, PT, P, I32, P, I32, I32, F32, P, P, P, P], ctypes.c_int),
     "msgl_read_status": ([P, ctypes.POINTER(ctypes.c_uint32), P], ctypes.c_int),
     "msgl_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "msgl_last_error": ([], ctypes.c_char_p),
@@ -222,6 +223,32 @@ def attn_extend(pool: KVPool, q: torch.Tensor, page_table: torch.Tensor, prefix_
         0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(status),
         _stream(stream))
     _check(rc, "msgl_attn_extend")
+    return out, lse
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def attn_decode_noalloc(pool: KVPool, q: torch.Tensor, page_table: torch.Tensor,
+                        seq_lens: torch.Tensor, max_seq_len: int, scale: float,
+                        out: torch.Tensor, lse: torch.Tensor,
+                        status: Optional[torch.Tensor] = None, stream=None):
+    """Decode with the library's built-in scratch instead of a workspace.
+
+    For callers that must not allocate device memory: the caller passes the
+    output buffers, and the library allocates nothing.  Same results as
+    :func:`attn_decode`.
+    """
+    _need(q, "q", torch.bfloat16)
+    _need(seq_lens, "seq_lens", torch.int32)
+    _need(out, "out", torch.bfloat16)
+    _need(lse, "lse", torch.float32)
+    B, hq, _ = q.shape
+    pc, pt = pool.c(), _pages(page_table)
+    rc = load().msgl_attn_decode_noalloc(
+        ctypes.byref(pc), ctypes.byref(pt), _ptr(q), hq, _ptr(seq_lens), B, int(max_seq_len),
+        float(scale), _ptr(out), _ptr(lse), _ptr(status), _stream(stream))
+    _check(rc, "msgl_attn_decode_noalloc")
     return out, lse
 
 
