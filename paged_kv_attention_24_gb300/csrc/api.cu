@@ -154,14 +154,14 @@ msgl_status msgl_attn_decode(const msgl_kv_pool *pool, const msgl_page_table *pa
     if (max_seq_len <= 0) return fail(MSGL_ERR_INVALID_ARG, "max_seq_len must be > 0");
     if (!q || !seq_lens || !o || !lse) return fail(MSGL_ERR_INVALID_ARG, "q, seq_lens, o and lse must be non-NULL");
     if (!aligned16(q) || !aligned16(o)) return fail(MSGL_ERR_INVALID_ARG, "q and o must be 16-byte aligned");
+    if (pool->num_kv_heads > 8 && pool->num_kv_heads % 8 != 0)
+        return fail(MSGL_ERR_UNSUPPORTED, "decode needs num_kv_heads <= 8 or a multiple of 8");
     const msgl::DecodePlan plan = msgl::plan_decode(num_reqs, num_q_heads, pool->num_kv_heads, max_seq_len);
-    if (plan.num_splits > 1) {
-        if (!workspace || workspace_bytes < plan.workspace)
-            return fail(MSGL_ERR_WORKSPACE, "decode needs %zu workspace bytes, got %zu", plan.workspace,
-                        workspace ? workspace_bytes : (size_t)0);
-        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-            return fail(MSGL_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-    }
+    if (!workspace || workspace_bytes < plan.workspace)
+        return fail(MSGL_ERR_WORKSPACE, "decode needs %zu workspace bytes, got %zu", plan.workspace,
+                    workspace ? workspace_bytes : (size_t)0);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(MSGL_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     msgl::DecodeArgs a{};
     a.pool = pv;
     a.pages = pg;
@@ -173,11 +173,8 @@ msgl_status msgl_attn_decode(const msgl_kv_pool *pool, const msgl_page_table *pa
     a.scale = scale;
     a.o = static_cast<__nv_bfloat16 *>(o);
     a.lse = lse;
-    const size_t n_part = (size_t)num_reqs * num_q_heads * (size_t)plan.num_splits;
     a.part_o = static_cast<float *>(workspace);
-    a.part_lse = workspace ? reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                                       (n_part * msgl::kHeadDim * sizeof(float) + 255) / 256 * 256)
-                           : nullptr;
+    a.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.o_bytes);
     a.status = status;
     cudaError_t e = msgl::launch_decode(a, plan, (cudaStream_t)stream);
     return e == cudaSuccess ? MSGL_OK : cuda_fail(e, "decode launch");

@@ -1,109 +1,511 @@
-// Decode step: one query row per request over all of its pages, with the
-// keys split into chunks that run in parallel and a log-sum-exp merge.
+// Decode step: one query row per request over all of its pages.
 //
 // "Mini-SGLang 实战指南", §6.3: decode has its own attention kernel, apart
 // from prefill; §6.4: decode is replayed under CUDA graphs, so the launch
-// shape depends only on host scalars (num_reqs, max_seq_len); chunks past a
-// request's length exit at once.
+// shape depends only on host scalars and the device (never on seq_lens).
+//
+// Design (bandwidth-bound: every cached K/V byte is read exactly once)
+// ---------------------------------------------------------------------
+// * Balanced split-KV.  The keys of all requests, laid end to end, are cut
+//   into P equal ranges, one per persistent CTA (P = resident CTAs on the
+//   GPU).  A CTA's range covers one or more request segments; each segment
+//   yields a partial (o, lse) per q head.  Request b's partials sit in rows
+//   b + i of the workspace, i over the CTAs whose ranges touch it, and the
+//   merge kernel folds them together by their log-sum-exp.
+// * One CTA handles a group of up to 8 kv heads (all of them for Hkv <= 8),
+//   so each key's pool row (Hkv * 256 bytes, contiguous in the slot-major
+//   pool) arrives in one bulk copy.  A producer warp resolves slots through
+//   the page table (range-checked) and issues one cp.async.bulk per key for
+//   K and one for V into a ring of 16-key stages; rows land at a pitch of
+//   row + 16 bytes so that ldmatrix over 8 consecutive keys is free of bank
+//   conflicts.  Stages are handed over with mbarriers (full: bytes landed;
+//   empty: every consumer warp is done with the stage).
+// * One consumer warp per kv head computes S^T = K Q^T with m16n8k16 MMAs
+//   (M = 16 keys, N = the group's 8 q-head slots, K = 128 dims), keeps a
+//   base-2 online softmax per q head, transposes P to the B operand with
+//   movmatrix, and accumulates O^T = V^T P^T (M = 16 dims x 8 tiles).
+//   Packing the q heads of a kv head into N means each KV byte feeds all G
+//   q heads at once.
 #include <math.h>
 
 #include "kernels.h"
-#include "rows_kernel.cuh"
+#include "ptx.cuh"
 
 namespace msgl {
 
-DecodePlan plan_decode(int32_t num_reqs, int32_t hq, int32_t hkv, int32_t max_seq_len) {
-    DecodePlan p;
-    const int64_t per_split = (int64_t)num_reqs * hkv;
-    const int64_t target = 152 * 8;   // resident 128-thread CTAs on a full GPU
-    int64_t splits = per_split > 0 ? (target + per_split - 1) / per_split : 1;
-    const int64_t max_useful = ((int64_t)max_seq_len + 255) / 256;
-    if (splits > max_useful) splits = max_useful;
-    if (splits < 1) splits = 1;
-    int64_t chunk = ((int64_t)max_seq_len + splits - 1) / splits;
-    chunk = (chunk + 63) / 64 * 64;
-    if (chunk < 64) chunk = 64;
-    splits = ((int64_t)max_seq_len + chunk - 1) / chunk;
-    if (splits < 1) splits = 1;
-    p.num_splits = (int32_t)splits;
-    p.chunk = (int32_t)chunk;
-    const size_t n_part = (size_t)num_reqs * hq * (size_t)splits;
-    const size_t o_bytes = (n_part * kHeadDim * sizeof(float) + 255) / 256 * 256;
-    const size_t l_bytes = (n_part * sizeof(float) + 255) / 256 * 256;
-    p.workspace = splits > 1 ? o_bytes + l_bytes : 0;   // one chunk writes o/lse directly
-    return p;
+namespace {
+
+constexpr int kTileKeys = 16;
+constexpr int kMaxStages = 8;
+constexpr int kMaxDecodeCtas = 512;       // bound on P, used to size the workspace
+constexpr int kMaxHeadGroup = 8;
+constexpr int kSmemBudget = 220 * 1024;
+
+enum TileFlags { kFirst = 1, kLast = 2, kBad = 4, kEnd = 8 };
+
+struct TileMeta {
+    int32_t b;        // request
+    int32_t slot;     // partial row (b + CTA index)
+    int32_t n;        // keys in this tile
+    int32_t flags;
+    uint32_t mask;    // bit k: key k was loaded
+    int32_t pad[3];
+};
+
+struct DecodeKernelArgs {
+    PoolView pool;
+    PageView pages;
+    const __nv_bfloat16 *q;
+    const int32_t *seq_lens;
+    int32_t num_reqs, hq, group, max_seq_len, hg, stages;
+    float scale_log2;
+    float *part_o;
+    float *part_lse;
+    uint32_t *status;
+};
+
+__device__ __forceinline__ int seq_valid(const int32_t *seq_lens, int b, int max_seq) {
+    const int s = __ldg(seq_lens + b);
+    return (s >= 1 && s <= max_seq) ? s : 0;
 }
 
-// Merge the chunk partials of one (request, q head): weights exp(lse_s - max),
-// o = sum w_s o_s / sum w_s, lse = max + ln(sum w_s).  A NaN partial lse marks
-// a chunk that hit a bad index: the whole row is written as o = 0, lse = -inf.
-__global__ void __launch_bounds__(kHeadDim) decode_merge_kernel(
-    const float *__restrict__ part_o, const float *__restrict__ part_lse, int32_t num_splits,
-    int32_t hq, __nv_bfloat16 *__restrict__ o, float *__restrict__ lse) {
-    const int64_t bh = blockIdx.x;
-    const int d = threadIdx.x;
-    const float *pl = part_lse + bh * num_splits;
+__device__ __forceinline__ long long warp_incl_scan(long long v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+    }
+    return v;
+}
+
+size_t stage_bytes(int hg) { return (size_t)2 * kTileKeys * (hg * 256 + 16); }
+
+size_t decode_smem_bytes(int hg, int stages) {
+    return stages * stage_bytes(hg) + stages * sizeof(TileMeta) + 2 * stages * sizeof(uint64_t) + 16;
+}
+
+__global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
+    decode_split_kernel(const DecodeKernelArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int hg = a.hg;
+    const int pitch = hg * 256 + 16;
+    const int sbytes = 2 * kTileKeys * pitch;
+    const int S = a.stages;
+    TileMeta *meta = reinterpret_cast<TileMeta *>(smem + (size_t)S * sbytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(meta + S);
+    uint64_t *empty = full + S;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + S);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g0 = blockIdx.y * hg;   // first kv head of this CTA
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(ptx::smem_u32(full + s), 1);
+            ptx::mbar_init(ptx::smem_u32(empty + s), hg);
+        }
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == hg) {
+        // ------------------------------------------------------------ producer
+        const int B = a.num_reqs;
+        long long total = 0;
+        for (int c = 0; c < B; c += 32) {
+            const int s = (c + lane < B) ? seq_valid(a.seq_lens, c + lane, a.max_seq_len) : 0;
+            total += s;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+        const long long P = gridDim.x;
+        const long long per = (total + P - 1) / P;
+        const long long r0 = per * blockIdx.x;
+        const long long r1 = min(total, r0 + per);
+        int it = 0;
+        bool aborted = false;
+        const uint32_t row_bytes = (uint32_t)hg * 256;
+        const long long slot_elems = (long long)a.pool.hkv * kHeadDim;
+
+        auto stage_wait_empty = [&](int stage, int round) -> bool {
+            if (ptx::mbar_wait(ptx::smem_u32(empty + stage), (round & 1) ^ 1)) return true;
+            if (lane == 0) { report(a.status, MSGL_DEVERR_TIMEOUT); *abort_flag = 1; }
+            return false;
+        };
+
+        if (r0 < r1) {
+            // locate the request holding key r0
+            long long base = 0, start_b = 0;
+            int b = -1;
+            for (int c = 0; c < B && b < 0; c += 32) {
+                const int s = (c + lane < B) ? seq_valid(a.seq_lens, c + lane, a.max_seq_len) : 0;
+                const long long incl = warp_incl_scan(s, lane);
+                const long long tot = __shfl_sync(0xffffffffu, incl, 31);
+                if (r0 < base + tot) {
+                    const unsigned m = __ballot_sync(0xffffffffu, base + incl > r0);
+                    const int l = __ffs(m) - 1;
+                    b = c + l;
+                    start_b = base + __shfl_sync(0xffffffffu, incl - s, l);
+                }
+                base += tot;
+            }
+            long long pos = r0;
+            while (b >= 0 && b < B && pos < r1 && !aborted) {
+                const int sb = seq_valid(a.seq_lens, b, a.max_seq_len);
+                const long long end_b = start_b + sb;
+                if (end_b > pos) {
+                    const int lo = (int)(pos - start_b);
+                    const int hi = (int)(min(r1, end_b) - start_b);
+                    for (int t0 = lo; t0 < hi; t0 += kTileKeys) {
+                        const int stage = it % S, round = it / S;
+                        if (*abort_flag || !stage_wait_empty(stage, round)) { aborted = true; break; }
+                        const int n = min(kTileKeys, hi - t0);
+                        bool ok = false;
+                        int64_t slot = -1;
+                        if (lane < n) {
+                            bool bad = false;
+                            slot = slot_of(a.pool, a.pages, b, t0 + lane, bad);
+                            ok = !bad;
+                        }
+                        const uint32_t mask = __ballot_sync(0xffffffffu, ok);
+                        const uint32_t badm = __ballot_sync(0xffffffffu, lane < n && !ok);
+                        const uint32_t full_bar = ptx::smem_u32(full + stage);
+                        if (lane == 0) {
+                            TileMeta &md = meta[stage];
+                            md.b = b;
+                            md.slot = b + (int)blockIdx.x;
+                            md.n = n;
+                            md.flags = (t0 == lo ? kFirst : 0) | (t0 + kTileKeys >= hi ? kLast : 0) |
+                                       (badm ? kBad : 0);
+                            md.mask = mask;
+                            if (badm) report(a.status, MSGL_DEVERR_PAGE_RANGE);
+                            ptx::mbar_arrive_expect_tx(full_bar, __popc(mask) * row_bytes * 2);
+                        }
+                        __syncwarp();
+                        if (ok) {
+                            uint8_t *kdst = smem + (size_t)stage * sbytes + lane * pitch;
+                            uint8_t *vdst = kdst + kTileKeys * pitch;
+                            const long long off = slot * slot_elems + (long long)g0 * kHeadDim;
+                            ptx::bulk_g2s(ptx::smem_u32(kdst), a.pool.k + off, row_bytes, full_bar);
+                            ptx::bulk_g2s(ptx::smem_u32(vdst), a.pool.v + off, row_bytes, full_bar);
+                        }
+                        ++it;
+                    }
+                    pos = min(r1, end_b);
+                }
+                start_b = end_b;
+                ++b;
+            }
+        }
+        // end marker: an empty stage the consumers stop at
+        if (!aborted) {
+            const int stage = it % S, round = it / S;
+            if (!*abort_flag && stage_wait_empty(stage, round)) {
+                if (lane == 0) {
+                    meta[stage].flags = kEnd;
+                    ptx::mbar_arrive(ptx::smem_u32(full + stage));
+                }
+                ++it;
+            } else {
+                aborted = true;
+            }
+        }
+        if (aborted) {
+            // let every copy already issued land before the CTA exits (bounded)
+            const int first = it > S ? it - S : 0;
+            for (int k = first; k < it; ++k)
+                ptx::mbar_wait(ptx::smem_u32(full + (k % S)), (k / S) & 1, 200000000LL);
+        }
+    } else if (warp < hg) {
+        // ----------------------------------------------------------- consumers
+        const int g = g0 + warp;                 // this warp's kv head
+        const int G = a.group;
+        const int qh = lane >> 2;                // q-head slot this lane loads for Q^T
+        const int h0 = 2 * (lane & 3), h1 = h0 + 1;
+        const int k0 = lane >> 2, k1 = k0 + 8;   // keys of this lane's S^T elements
+        const int kv0 = 2 * (lane & 3), kv1 = kv0 + 8;  // keys of this lane's V^T fragment
+        uint32_t qf[8][2];
+        float acc[8][4];
+        float m2[2], l[2];
+        bool seg_bad = false;
+        const uint32_t tiles = ptx::smem_u32(smem);
+        // ldmatrix row addresses (per lane) inside a stage
+        const int krow = (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int kcol = 8 * (lane >> 4);
+        const int vrow = (lane & 7) + 8 * (lane >> 4);
+        const int vcol = 8 * ((lane >> 3) & 1);
+        const uint32_t k_lane = (uint32_t)(krow * pitch + warp * 256 + kcol * 2);
+        const uint32_t v_lane = (uint32_t)(kTileKeys * pitch + vrow * pitch + warp * 256 + vcol * 2);
+
+        for (int it = 0;; ++it) {
+            const int stage = it % S, round = it / S;
+            if (*abort_flag) break;
+            if (!ptx::mbar_wait(ptx::smem_u32(full + stage), round & 1)) {
+                if (lane == 0) { report(a.status, MSGL_DEVERR_TIMEOUT); *abort_flag = 1; }
+                break;
+            }
+            const int flags = meta[stage].flags;
+            if (flags & kEnd) break;
+            const int b = meta[stage].b;
+            const int pslot = meta[stage].slot;
+            const uint32_t mask = meta[stage].mask;
+
+            if (flags & kFirst) {
+                const __nv_bfloat16 *qp = a.q + ((long long)b * a.hq + (long long)g * G + qh) * kHeadDim;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    if (qh < G) {
+                        qf[ks][0] = *reinterpret_cast<const uint32_t *>(qp + 16 * ks + 2 * (lane & 3));
+                        qf[ks][1] = *reinterpret_cast<const uint32_t *>(qp + 16 * ks + 8 + 2 * (lane & 3));
+                    } else {
+                        qf[ks][0] = qf[ks][1] = 0u;
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+                m2[0] = m2[1] = -INFINITY;
+                l[0] = l[1] = 0.f;
+                seg_bad = false;
+            }
+            seg_bad |= (flags & kBad) != 0;
+
+            const uint32_t base = tiles + (uint32_t)(stage * sbytes);
+            // S^T (16 keys x 8 q-head slots) = K (16 x 128) * Q^T (128 x 8)
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                uint32_t af[4];
+                ptx::ldsm_x4(base + k_lane + ks * 32, af[0], af[1], af[2], af[3]);
+                ptx::mma_bf16_16816(s, af, qf[ks][0], qf[ks][1]);
+            }
+            const bool v0 = (mask >> k0) & 1u, v1 = (mask >> k1) & 1u;
+            const float x00 = v0 ? s[0] * a.scale_log2 : -INFINITY;   // key k0, head h0
+            const float x01 = v0 ? s[1] * a.scale_log2 : -INFINITY;   // key k0, head h1
+            const float x10 = v1 ? s[2] * a.scale_log2 : -INFINITY;   // key k1, head h0
+            const float x11 = v1 ? s[3] * a.scale_log2 : -INFINITY;   // key k1, head h1
+            float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float mn0 = fmaxf(m2[0], mx0), mn1 = fmaxf(m2[1], mx1);
+            const float al0 = (mn0 == -INFINITY) ? 1.f : exp2f(m2[0] - mn0);
+            const float al1 = (mn1 == -INFINITY) ? 1.f : exp2f(m2[1] - mn1);
+            const float p00 = (x00 == -INFINITY) ? 0.f : exp2f(x00 - mn0);
+            const float p01 = (x01 == -INFINITY) ? 0.f : exp2f(x01 - mn1);
+            const float p10 = (x10 == -INFINITY) ? 0.f : exp2f(x10 - mn0);
+            const float p11 = (x11 == -INFINITY) ? 0.f : exp2f(x11 - mn1);
+            m2[0] = mn0;
+            m2[1] = mn1;
+            l[0] = l[0] * al0 + p00 + p10;
+            l[1] = l[1] * al1 + p01 + p11;
+            const uint32_t pb0 = ptx::movmatrix_t(ptx::pack_bf16(p00, p01));   // keys 0-7
+            const uint32_t pb1 = ptx::movmatrix_t(ptx::pack_bf16(p10, p11));   // keys 8-15
+            // zero V^T fragment entries of keys that were not loaded
+            const uint32_t ma = ((mask >> kv0) & 1u ? 0x0000ffffu : 0u) | ((mask >> (kv0 + 1)) & 1u ? 0xffff0000u : 0u);
+            const uint32_t mb = ((mask >> kv1) & 1u ? 0x0000ffffu : 0u) | ((mask >> (kv1 + 1)) & 1u ? 0xffff0000u : 0u);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                uint32_t af[4];
+                ptx::ldsm_x4_t(base + v_lane + i * 32, af[0], af[1], af[2], af[3]);
+                af[0] &= ma;
+                af[1] &= ma;
+                af[2] &= mb;
+                af[3] &= mb;
+                acc[i][0] *= al0;
+                acc[i][1] *= al1;
+                acc[i][2] *= al0;
+                acc[i][3] *= al1;
+                ptx::mma_bf16_16816(acc[i], af, pb0, pb1);
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(empty + stage));
+
+            if (flags & kLast) {
+                float lt0 = l[0], lt1 = l[1];
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    lt0 += __shfl_xor_sync(0xffffffffu, lt0, o);
+                    lt1 += __shfl_xor_sync(0xffffffffu, lt1, o);
+                }
+                const float inv0 = lt0 > 0.f ? 1.f / lt0 : 0.f;
+                const float inv1 = lt1 > 0.f ? 1.f / lt1 : 0.f;
+                const long long hb = (long long)pslot * a.hq + (long long)g * G;
+                float *po = a.part_o + hb * kHeadDim;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int d0 = 16 * i + (lane >> 2), d1 = d0 + 8;
+                    if (h0 < G) {
+                        po[h0 * kHeadDim + d0] = acc[i][0] * inv0;
+                        po[h0 * kHeadDim + d1] = acc[i][2] * inv0;
+                    }
+                    if (h1 < G) {
+                        po[h1 * kHeadDim + d0] = acc[i][1] * inv1;
+                        po[h1 * kHeadDim + d1] = acc[i][3] * inv1;
+                    }
+                }
+                if (lane < 4) {
+                    const float nan = __int_as_float(0x7fc00000);
+                    if (h0 < G)
+                        a.part_lse[hb + h0] = (seg_bad || !(lt0 > 0.f)) ? nan : (m2[0] + log2f(lt0)) * kLn2;
+                    if (h1 < G)
+                        a.part_lse[hb + h1] = (seg_bad || !(lt1 > 0.f)) ? nan : (m2[1] + log2f(lt1)) * kLn2;
+                }
+            }
+        }
+    }
+    __syncthreads();
+}
+
+// Fold the partials of request b, q head h: weights exp(lse_i - max),
+// o = sum w_i o_i / sum w_i, lse = max + ln(sum w_i).  A NaN partial lse
+// marks a segment that hit a bad index: the row is written as o = 0, lse = -inf.
+__global__ void __launch_bounds__(256) decode_merge_kernel(
+    const int32_t *__restrict__ seq_lens, int32_t num_reqs, int32_t max_seq_len, int32_t hq,
+    int32_t num_ctas, const float *__restrict__ part_o, const float *__restrict__ part_lse,
+    __nv_bfloat16 *__restrict__ o, float *__restrict__ lse, uint32_t *status) {
+    __shared__ long long s_start, s_total;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.y;
+    if (warp == 0) {
+        long long total = 0, before = 0;
+        for (int c = 0; c < num_reqs; c += 32) {
+            const int idx = c + lane;
+            const int s = idx < num_reqs ? seq_valid(seq_lens, idx, max_seq_len) : 0;
+            total += s;
+            if (idx < b) before += s;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            total += __shfl_xor_sync(0xffffffffu, total, off);
+            before += __shfl_xor_sync(0xffffffffu, before, off);
+        }
+        if (lane == 0) { s_total = total; s_start = before; }
+    }
+    __syncthreads();
+    const int h = blockIdx.x * 8 + warp;
+    if (h >= hq) return;
+    const int sb = seq_valid(seq_lens, b, max_seq_len);
+    const long long row = (long long)b * hq + h;
+    __nv_bfloat16 *orow = o + row * kHeadDim + lane * 4;
+    if (sb == 0) {
+        if (blockIdx.x == 0 && warp == 0 && lane == 0) report(status, MSGL_DEVERR_LENGTH);
+        *reinterpret_cast<uint2 *>(orow) = make_uint2(0u, 0u);
+        if (lane == 0) lse[row] = -INFINITY;
+        return;
+    }
+    const long long per = (s_total + num_ctas - 1) / num_ctas;
+    const int first = (int)(s_start / per);
+    const int last = (int)((s_start + sb - 1) / per);
     float M = -INFINITY;
     bool failed = false;
-    for (int s = 0; s < num_splits; ++s) {
-        const float x = pl[s];
+    for (int i = first; i <= last; ++i) {
+        const float x = part_lse[(long long)(b + i) * hq + h];
         if (isnan(x)) failed = true;
         else M = fmaxf(M, x);
     }
-    float L = 0.f, O = 0.f;
+    float L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
     if (!failed && M != -INFINITY) {
-        for (int s = 0; s < num_splits; ++s) {
-            const float x = pl[s];
-            if (x == -INFINITY) continue;
-            const float w = __expf(x - M);
+        for (int i = first; i <= last; ++i) {
+            const long long pr = (long long)(b + i) * hq + h;
+            const float w = __expf(part_lse[pr] - M);
+            const float4 v = *reinterpret_cast<const float4 *>(part_o + pr * kHeadDim + lane * 4);
             L += w;
-            O += w * part_o[(bh * num_splits + s) * kHeadDim + d];
+            acc[0] += w * v.x;
+            acc[1] += w * v.y;
+            acc[2] += w * v.z;
+            acc[3] += w * v.w;
         }
     }
-    const bool zero = failed || L == 0.f;
-    o[bh * kHeadDim + d] = __float2bfloat16_rn(zero ? 0.f : O / L);
-    if (d == 0) lse[bh] = zero ? -INFINITY : M + logf(L);
+    const bool zero = failed || !(L > 0.f);
+    const float inv = zero ? 0.f : 1.f / L;
+    const uint32_t lo = ptx::pack_bf16(acc[0] * inv, acc[1] * inv);
+    const uint32_t hi = ptx::pack_bf16(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2 *>(orow) = make_uint2(lo, hi);
+    if (lane == 0) lse[row] = zero ? -INFINITY : M + logf(L);
 }
 
-template <int G>
-static void launch_rows_decode(const RowsArgs &r, dim3 grid, cudaStream_t stream) {
-    attn_rows_kernel<G, false><<<grid, kRowsWarps * 32, 0, stream>>>(r);
+struct Launch {
+    int hg, stages, ctas;
+    size_t smem;
+};
+
+Launch decode_launch_shape(int hkv) {
+    Launch L;
+    L.hg = hkv <= kMaxHeadGroup ? hkv : kMaxHeadGroup;
+    int st = (int)((kSmemBudget - 64) / (stage_bytes(L.hg) + sizeof(TileMeta) + 16));
+    L.stages = st < 2 ? 2 : (st > kMaxStages ? kMaxStages : st);
+    L.smem = decode_smem_bytes(L.hg, L.stages);
+    static int sm_count[64];   // per device, filled on first use (same value if two threads race)
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int sms = (dev >= 0 && dev < 64) ? sm_count[dev] : 0;
+    if (sms == 0) {
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 1;
+        if (dev >= 0 && dev < 64) sm_count[dev] = sms;
+    }
+    const int groups = hkv / L.hg;
+    int ctas = sms / groups;
+    if (ctas < 1) ctas = 1;
+    L.ctas = ctas > kMaxDecodeCtas ? kMaxDecodeCtas : ctas;
+    return L;
+}
+
+}  // namespace
+
+DecodePlan plan_decode(int32_t num_reqs, int32_t hq, int32_t hkv, int32_t max_seq_len) {
+    (void)max_seq_len;
+    (void)hkv;
+    DecodePlan p;
+    const size_t rows = (size_t)num_reqs + kMaxDecodeCtas;
+    p.o_bytes = (rows * hq * kHeadDim * sizeof(float) + 255) / 256 * 256;
+    const size_t l_bytes = (rows * hq * sizeof(float) + 255) / 256 * 256;
+    p.workspace = p.o_bytes + l_bytes;
+    return p;
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream) {
     if (a.num_reqs == 0) return cudaSuccess;
-    RowsArgs r{};
-    r.pool = a.pool;
-    r.pages = a.pages;
-    r.q = a.q;
-    r.hq = a.hq;
-    r.scale_log2 = a.scale * kLog2e;
-    r.seq_lens = a.seq_lens;
-    r.max_seq_len = a.max_seq_len;
-    r.chunk = plan.chunk;
-    r.num_splits = plan.num_splits;
-    r.o = a.o;
-    r.lse = a.lse;
-    r.part_o = a.part_o;
-    r.part_lse = a.part_lse;
-    r.status = a.status;
-    const int G = a.hq / a.pool.hkv;
-    dim3 grid(plan.num_splits, a.pool.hkv, a.num_reqs);
-    switch (G) {
-        case 1: launch_rows_decode<1>(r, grid, stream); break;
-        case 2: launch_rows_decode<2>(r, grid, stream); break;
-        case 3: launch_rows_decode<3>(r, grid, stream); break;
-        case 4: launch_rows_decode<4>(r, grid, stream); break;
-        case 5: launch_rows_decode<5>(r, grid, stream); break;
-        case 6: launch_rows_decode<6>(r, grid, stream); break;
-        case 7: launch_rows_decode<7>(r, grid, stream); break;
-        case 8: launch_rows_decode<8>(r, grid, stream); break;
-        default: return cudaErrorInvalidValue;
+    const int hkv = a.pool.hkv;
+    if (hkv > kMaxHeadGroup && hkv % kMaxHeadGroup != 0) return cudaErrorInvalidValue;
+    const Launch L = decode_launch_shape(hkv);
+    static bool attr_set[64];   // per device; idempotent, racing setters write the same value
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(decode_split_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmemBudget);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
+    DecodeKernelArgs k{};
+    k.pool = a.pool;
+    k.pages = a.pages;
+    k.q = a.q;
+    k.seq_lens = a.seq_lens;
+    k.num_reqs = a.num_reqs;
+    k.hq = a.hq;
+    k.group = a.hq / hkv;
+    k.max_seq_len = a.max_seq_len;
+    k.hg = L.hg;
+    k.stages = L.stages;
+    k.scale_log2 = a.scale * kLog2e;
+    k.part_o = a.part_o;
+    k.part_lse = a.part_lse;
+    k.status = a.status;
+    (void)plan;
+    if (L.smem > (size_t)kSmemBudget) return cudaErrorInvalidValue;
+    dim3 grid(L.ctas, hkv / L.hg);
+    decode_split_kernel<<<grid, 32 * (L.hg + 1), L.smem, stream>>>(k);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || plan.num_splits == 1) return e;
-    decode_merge_kernel<<<(unsigned)((int64_t)a.num_reqs * a.hq), kHeadDim, 0, stream>>>(
-        a.part_o, a.part_lse, plan.num_splits, a.hq, a.o, a.lse);
+    if (e != cudaSuccess) return e;
+    dim3 mgrid((a.hq + 7) / 8, a.num_reqs);
+    decode_merge_kernel<<<mgrid, 256, 0, stream>>>(a.seq_lens, a.num_reqs, a.max_seq_len, a.hq, L.ctas,
+                                                   a.part_o, a.part_lse, a.o, a.lse, a.status);
     return cudaGetLastError();
 }
 

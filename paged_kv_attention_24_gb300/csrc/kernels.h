@@ -17,9 +17,8 @@ cudaError_t launch_store_kv(const PoolView &pool, __nv_bfloat16 *k_pool, __nv_bf
 
 // --------------------------------------------------------------- decode
 struct DecodePlan {
-    int32_t num_splits;   // key chunks per request
-    int32_t chunk;        // keys per chunk (multiple of 64)
-    size_t workspace;     // bytes of split partials
+    size_t o_bytes;       // bytes of the fp32 partial outputs (start of the workspace)
+    size_t workspace;     // total bytes: partial outputs, then partial LSEs
 };
 DecodePlan plan_decode(int32_t num_reqs, int32_t hq, int32_t hkv, int32_t max_seq_len);
 
@@ -32,8 +31,8 @@ struct DecodeArgs {
     float scale;
     __nv_bfloat16 *o;
     float *lse;
-    float *part_o;      // [num_reqs, hq, num_splits, 128]
-    float *part_lse;    // [num_reqs, hq, num_splits]
+    float *part_o;      // [num_reqs + max CTAs, hq, 128] segment partials
+    float *part_lse;    // [num_reqs + max CTAs, hq]
     uint32_t *status;
 };
 cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream);
