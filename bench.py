@@ -77,7 +77,7 @@ def kernel_source_sha(files):
 
 KERNEL_SOURCES = {
     "decode": ["decode.cu", "ptx.cuh", "common.cuh"],
-    "extend": ["extend.cu", "rows_kernel.cuh", "common.cuh"],
+    "extend": ["extend.cu", "ptx.cuh", "common.cuh"],
     "store": ["store_kv.cu", "common.cuh"],
 }
 

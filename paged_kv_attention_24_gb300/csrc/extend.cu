@@ -1,51 +1,544 @@
-// Extend (chunked prefill) step: chunk row i of request b attends keys
-// 0..prefix_b + i of the request's pages ("Mini-SGLang 实战指南", §6.1
-// "Chunked Prefill" and §6.5 "Radix Cache": a chunk runs over the cached
-// prefix plus its own causal part).
+// Extend (chunked prefill) step on the 5th-generation tensor cores.
+//
+// Chunk row i of request b attends keys 0..prefix_b + i of the request's
+// pages: the cached (radix-shared) prefix plus its own causal part
+// ("Mini-SGLang 实战指南", §6.1 "Chunked Prefill" and §6.5 "Radix Cache";
+// "不懂SGLang？从miniSGLang开始", §1.3: K/V come from the pool, located
+// through the page table).
+//
+// Design
+// ------
+// * GQA packing: a 128-row Q tile holds R = floor(128 / G) consecutive
+//   tokens x the G q heads of one kv head (row r = token r / G, head r % G),
+//   loaded by one 3D TMA box per 64-dim half straight from q[T, Hq, 128].
+//   Every K/V byte staged in shared memory feeds all G heads.
+// * A CTA owns two such tiles (2R tokens) of one request and one kv head and
+//   streams 128-key K and V tiles through a 2-stage ring.  A page that is a
+//   contiguous, fully valid run of pool rows (page_size >= 16) arrives in one
+//   tiled TMA box per 64-dim half; any other keys are gathered four pool
+//   rows per copy (TMA gather4).  A key beyond the causal range, or behind a
+//   bad page id, gets a row index past the end of the pool, which TMA fills
+//   with zeros.
+// * tcgen05.mma (M = N = 128, K = 16 per instruction, bf16 in, fp32 out):
+//   S_t = Q_t K^T lands in TMEM (columns 0-127 for tile 0, 128-255 for tile
+//   1); O_t accumulates in columns 256-383 / 384-511 (the whole 512-column
+//   TMEM of the SM).  P is written back over S_t as packed bf16 and fed to
+//   O_t += P_t V from TMEM, with V as an MN-major shared-memory operand.
+// * Warp roles: warp 0 issues TMA, one thread of warp 1 issues the MMAs,
+//   warps 4-7 and 8-11 run the online softmax of tile 0 and tile 1 (one
+//   TMEM lane = one row per thread).  While one warpgroup exponentiates,
+//   the tensor core works on the other tile.  O is rescaled lazily: only
+//   when a row's running max grows by more than 2^8 (so P stays <= 256).
+// * Every mbarrier wait is bounded; a timeout sets MSGL_DEVERR_TIMEOUT and
+//   the CTA winds down after its copies and MMAs have landed.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <limits.h>
+#include <math.h>
+#include <string.h>
+
 #include "kernels.h"
-#include "rows_kernel.cuh"
+#include "ptx.cuh"
 
 namespace msgl {
 
-size_t extend_workspace_bytes(int32_t, int32_t, int32_t, int32_t, int32_t) { return 0; }
+namespace {
 
-template <int G>
-static void launch_rows_extend(const RowsArgs &r, dim3 grid, cudaStream_t stream) {
-    attn_rows_kernel<G, true><<<grid, kRowsWarps * 32, 0, stream>>>(r);
+constexpr int kRows = 128;                 // rows per Q tile (MMA M)
+constexpr int kKeys = 128;                 // keys per K/V tile (MMA N of S, K of PV)
+constexpr int kStages = 2;
+constexpr int kThreads = 384;              // 12 warps
+constexpr uint32_t kHalf = 16384;          // 128 rows x 128 bytes (64 bf16)
+constexpr uint32_t kTile = 2 * kHalf;      // 128 x 128 bf16
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + 2 * kTile;
+constexpr uint32_t kOffV = kOffK + kStages * kTile;
+constexpr uint32_t kOffBar = kOffV + kStages * kTile;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // + slack to align the base to 1024
+
+// barrier slots
+constexpr int kQFull = 0, kKFull = 1, kKEmpty = 3, kVFull = 5, kVEmpty = 7, kSFull = 9, kPFull = 11,
+              kOFull = 13, kDrain = 15, kNumBars = 16;
+
+struct ExtendKernelArgs {
+    PoolView pool;
+    PageView pages;
+    const int32_t *prefix_lens, *ext_lens, *cu_ext, *positions;
+    int32_t hq, group, rows_per_tile, q_box_rows, total_tokens, num_reqs, nblk, oob_row;
+    int32_t box_rows;     // rows of one tiled pool box (min(page_size, 128)); 0 = gather only
+    float scale_log2;
+    __nv_bfloat16 *o;
+    float *lse;
+    uint32_t *status;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                              uint32_t *status) {
+    if (ptx::mbar_wait(bar, parity)) return true;
+    report(status, MSGL_DEVERR_TIMEOUT);
+    *abort_flag = 1;
+    return false;
 }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    extend_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
+                     const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap kt_map,
+                     const __grid_constant__ CUtensorMap vt_map, const ExtendKernelArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ---- work item: heaviest token blocks first, then kv head, then request
+    const int per_rank = a.pool.hkv * a.num_reqs;
+    const int rank = blockIdx.x / per_rank;
+    const int rest = blockIdx.x - rank * per_rank;
+    const int g = rest % a.pool.hkv;
+    const int b = rest / a.pool.hkv;
+    const int blk = a.nblk - 1 - rank;
+    const int R = a.rows_per_tile, G = a.group;
+    const int ext = __ldg(a.ext_lens + b);
+    const int pre = __ldg(a.prefix_lens + b);
+    const int cu_b = __ldg(a.cu_ext + b);
+    const int i0 = blk * 2 * R;
+    if (blk == 0 && g == 0 && threadIdx.x == 0) {
+        if (ext > a.nblk * 2 * R || __ldg(a.cu_ext + b + 1) - cu_b != ext || pre < 0 || cu_b < 0 ||
+            (long long)cu_b + ext > a.total_tokens)
+            report(a.status, MSGL_DEVERR_LENGTH);
+    }
+    if (i0 >= ext || pre < 0 || cu_b < 0 || (long long)cu_b + ext > a.total_tokens) return;
+
+    const int nA = min(R, ext - i0);
+    const int nB = max(0, min(R, ext - i0 - R));
+    const int nkv0 = (pre + i0 + nA + kKeys - 1) / kKeys;          // K/V tiles tile 0 needs
+    const int nkv1 = nB > 0 ? (pre + i0 + R + nB + kKeys - 1) / kKeys : 0;
+    const int nkv = max(nkv0, nkv1);
+    const int nkeys = nB > 0 ? pre + i0 + R + nB : pre + i0 + nA;
+    const int tok0 = cu_b + i0;
+
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sbase - raw);
+    const uint32_t bar0 = sbase + kOffBar;
+    auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + kOffBar + 8 * kNumBars);
+    volatile int *min_bad = reinterpret_cast<volatile int *>(smem + kOffBar + 8 * kNumBars + 4);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffBar + 8 * kNumBars + 8);
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar(kQFull), 1);
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(bar(kKFull + s), 1);
+            ptx::mbar_init(bar(kKEmpty + s), 1);
+            ptx::mbar_init(bar(kVFull + s), 1);
+            ptx::mbar_init(bar(kVEmpty + s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(bar(kSFull + t), 1);
+            ptx::mbar_init(bar(kPFull + t), 4);
+            ptx::mbar_init(bar(kOFull + t), 1);
+        }
+        ptx::mbar_init(bar(kDrain), 1);
+        *min_bad = INT_MAX;
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 2) {
+        ptx::tc_alloc(ptx::smem_u32((const void *)tmem_slot), 512);
+        ptx::tc_relinquish();
+    }
+    if (warp == 2 || warp == 3) {
+        // zero the Q rows a TMA box does not cover (GQA padding rows)
+        const int used = a.q_box_rows * G;
+        const int pad_bytes = (kRows - used) * 128;
+        for (int t = 0; t < 2; ++t)
+            for (int h = 0; h < 2; ++h) {
+                uint8_t *p = smem + kOffQ + t * kTile + h * kHalf + used * 128;
+                for (int x = (threadIdx.x - 64) * 16; x < pad_bytes; x += 64 * 16)
+                    *reinterpret_cast<uint4 *>(p + x) = make_uint4(0, 0, 0, 0);
+            }
+        ptx::fence_proxy_async_smem();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            const uint32_t box = 64u * G * a.q_box_rows * 2u;
+            ptx::mbar_arrive_expect_tx(bar(kQFull), box * (nB > 0 ? 4u : 2u));
+            for (int t = 0; t < (nB > 0 ? 2 : 1); ++t)
+                for (int h = 0; h < 2; ++h)
+                    ptx::tma_load_3d(sbase + kOffQ + t * kTile + h * kHalf, &q_map, 64 * h, g * G,
+                                     tok0 + t * R, bar(kQFull));
+        }
+        int issued = 0;
+        // Keys come in 4-key groups, one per lane.  When a page is a contiguous run of
+        // pool rows (box_rows > 0), a fully valid box of box_rows keys is fetched by one
+        // tiled copy per 64-dim half, issued by the box's first lane; any other group is
+        // gathered four rows at a time, with out-of-range rows (zero fill) for keys past
+        // the causal range or behind a bad page id.
+        const int BR = a.box_rows;
+        const int lanes_per_box = BR > 0 ? BR / 4 : 1;
+        const int box_lead = (lane / lanes_per_box) * lanes_per_box;
+        const unsigned box_bits =
+            lanes_per_box >= 32 ? 0xffffffffu : ((1u << lanes_per_box) - 1u) << box_lead;
+        for (int j = 0; j < nkv && !*abort_flag; ++j) {
+            const int s = j & 1, rnd = j >> 1;
+            int rows[4];
+            bool all_ok = true;
+            int64_t slot0 = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int key = j * kKeys + 4 * lane + e;
+                rows[e] = a.oob_row;
+                if (key < nkeys) {
+                    bool badp = false;
+                    const int64_t slot = slot_of(a.pool, a.pages, b, key, badp);
+                    if (badp) {
+                        atomicMin((int *)min_bad, key);
+                        all_ok = false;
+                    } else {
+                        rows[e] = (int)(slot * a.pool.hkv + g);
+                        if (e == 0) slot0 = slot;
+                    }
+                } else {
+                    all_ok = false;
+                }
+            }
+            const unsigned ok_mask = __ballot_sync(0xffffffffu, all_ok);
+            const bool tiled = BR > 0 && (ok_mask & box_bits) == box_bits;
+            auto issue = [&](uint32_t dst, const CUtensorMap *gm, const CUtensorMap *tm, uint32_t fb) {
+                if (!tiled) {
+                    ptx::tma_gather4(dst, gm, 0, rows[0], rows[1], rows[2], rows[3], fb);
+                    ptx::tma_gather4(dst + kHalf, gm, 64, rows[0], rows[1], rows[2], rows[3], fb);
+                } else if (lane == box_lead) {
+                    ptx::tma_load_3d(dst, tm, 0, g, (int)slot0, fb);
+                    ptx::tma_load_3d(dst + kHalf, tm, 64, g, (int)slot0, fb);
+                }
+            };
+            if (!wait_or_abort(bar(kKEmpty + s), (rnd & 1) ^ 1, abort_flag, a.status)) break;
+            if (lane == 0) ptx::mbar_arrive_expect_tx(bar(kKFull + s), kTile);
+            __syncwarp();
+            issue(sbase + kOffK + s * kTile + lane * 512, &k_map, &kt_map, bar(kKFull + s));
+            if (!wait_or_abort(bar(kVEmpty + s), (rnd & 1) ^ 1, abort_flag, a.status)) { issued = j + 1; break; }
+            if (lane == 0) ptx::mbar_arrive_expect_tx(bar(kVFull + s), kTile);
+            __syncwarp();
+            issue(sbase + kOffV + s * kTile + lane * 512, &v_map, &vt_map, bar(kVFull + s));
+            issued = j + 1;
+        }
+        if (*abort_flag) {
+            // let issued copies land before shared memory goes away (bounded waits)
+            ptx::mbar_wait(bar(kQFull), 0, 200000000LL);
+            for (int j = max(0, issued - kStages); j < issued; ++j) {
+                ptx::mbar_wait(bar(kKFull + (j & 1)), (j >> 1) & 1, 200000000LL);
+                ptx::mbar_wait(bar(kVFull + (j & 1)), (j >> 1) & 1, 200000000LL);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = ptx::umma_idesc_bf16(128, 128, false, false);
+            constexpr uint32_t idesc_o = ptx::umma_idesc_bf16(128, 128, false, true);
+            bool ok = wait_or_abort(bar(kQFull), 0, abort_flag, a.status);
+            ptx::tc_fence_after();
+            for (int j = 0; ok && j < nkv; ++j) {
+                const int s = j & 1, ph = (j >> 1) & 1;
+                if (!(ok = wait_or_abort(bar(kKFull + s), ph, abort_flag, a.status))) break;
+                ptx::tc_fence_after();
+                const uint32_t kb = sbase + kOffK + s * kTile;
+                for (int t = 0; t < 2; ++t) {
+                    if (j >= (t ? nkv1 : nkv0)) continue;
+                    const uint32_t qb = sbase + kOffQ + t * kTile;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                        ptx::tc_mma_ss(tmem + 128 * t, ptx::umma_desc_sw128(qb + off, 16, 1024),
+                                       ptx::umma_desc_sw128(kb + off, 16, 1024), idesc_s, kk > 0);
+                    }
+                    ptx::tc_commit(bar(kSFull + t));
+                }
+                ptx::tc_commit(bar(kKEmpty + s));
+                if (!(ok = wait_or_abort(bar(kVFull + s), ph, abort_flag, a.status))) break;
+                ptx::tc_fence_after();
+                const uint32_t vb = sbase + kOffV + s * kTile;
+                for (int t = 0; t < 2; ++t) {
+                    if (j >= (t ? nkv1 : nkv0)) continue;
+                    if (!(ok = wait_or_abort(bar(kPFull + t), j & 1, abort_flag, a.status))) break;
+                    ptx::tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        ptx::tc_mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8,
+                                       ptx::umma_desc_sw128(vb + kk * 2048, kHalf, 1024), idesc_o,
+                                       (j > 0 || kk > 0) ? 1u : 0u);
+                    ptx::tc_commit(bar(kOFull + t));
+                }
+                if (!ok) break;
+                ptx::tc_commit(bar(kVEmpty + s));
+            }
+            // drain: every MMA issued above has completed once this fires
+            ptx::tc_commit(bar(kDrain));
+            ptx::mbar_wait(bar(kDrain), 0, 400000000LL);
+        }
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------------- softmax
+        const int t = (warp - 4) >> 2;                 // Q tile of this warpgroup
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;                // TMEM lane = tile row
+        const int tok_l = r / G, jh = r - tok_l * G;
+        const int n_t = t == 0 ? nA : nB;
+        const int i_row = i0 + t * R + tok_l;
+        const bool row_valid = (r < R * G) && (tok_l < n_t);
+        const int limit = pre + i_row;                 // last key this row may see
+        const int jm = (pre + i0 + t * R + 1) >> 7;    // tiles >= jm may need masking
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const uint32_t tS = tmem + lane_base + 128 * t;
+        const uint32_t tO = tmem + lane_base + 256 + 128 * t;
+        float m_ref = -INFINITY, l = 0.f;
+        const int my_nkv = t ? nkv1 : nkv0;
+        bool ok = true;
+        for (int j = 0; j < my_nkv; ++j) {
+            if (!(ok = wait_or_abort(bar(kSFull + t), j & 1, abort_flag, a.status))) break;
+            if (j > 0 && !(ok = wait_or_abort(bar(kOFull + t), (j - 1) & 1, abort_flag, a.status))) break;
+            ptx::tc_fence_after();
+            const bool masked = j >= jm;             // uniform: only tiles past the first row's limit
+            const int lim = limit - j * kKeys;       // key c of this tile is visible iff c <= lim
+            // pass 1: row max of the raw scores
+            float mxa = -INFINITY, mxb = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                ptx::tc_ld32(tS + 32 * c, v);
+                ptx::tc_wait_ld();
+                if (!masked) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        mxa = ptx::max3(mxa, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                        mxb = ptx::max3(mxb, __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const float x0 = (32 * c + i <= lim) ? __uint_as_float(v[i]) : -INFINITY;
+                        const float x1 = (32 * c + i + 1 <= lim) ? __uint_as_float(v[i + 1]) : -INFINITY;
+                        mxa = ptx::max3(mxa, x0, x1);
+                    }
+                }
+            }
+            const float m_new = fmaxf(m_ref, fmaxf(mxa, mxb) * a.scale_log2);
+            const bool need = m_new > m_ref + 8.f;
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                const float alpha = need ? ptx::ex2(m_ref - m_new) : 1.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    ptx::tc_ld32(tO + 32 * c, v);
+                    ptx::tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                    ptx::tc_st32(tO + 32 * c, v);
+                }
+                ptx::tc_wait_st();
+                l *= alpha;
+            }
+            if (need) m_ref = m_new;
+            // pass 2: P = 2^(s * scale_log2 - m_ref), written back over S as bf16 pairs
+            const uint64_t sc2 = ptx::f2_pack(a.scale_log2, a.scale_log2);
+            const uint64_t nm2 = ptx::f2_pack(-m_ref, -m_ref);
+            uint64_t l2 = ptx::f2_pack(0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                ptx::tc_ld32(tS + 32 * c, v);
+                ptx::tc_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const uint64_t x2 = ptx::f2_fma(
+                        ptx::f2_pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), sc2, nm2);
+                    float x0, x1;
+                    ptx::f2_unpack(x2, x0, x1);
+                    float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+                    if (masked) {
+                        p0 = (32 * c + 2 * i <= lim) ? p0 : 0.f;
+                        p1 = (32 * c + 2 * i + 1 <= lim) ? p1 : 0.f;
+                    }
+                    l2 = ptx::f2_add(l2, ptx::f2_pack(p0, p1));
+                    pk[i] = ptx::pack_bf16(p0, p1);
+                }
+                ptx::tc_st16(tS + 16 * c, pk);
+            }
+            {
+                float la, lb;
+                ptx::f2_unpack(l2, la, lb);
+                l += la + lb;
+            }
+            ptx::tc_wait_st();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(kPFull + t));
+        }
+        // epilogue: O / l -> bf16, lse = ln(sum exp(s))
+        if (ok && my_nkv > 0 && wait_or_abort(bar(kOFull + t), (my_nkv - 1) & 1, abort_flag, a.status)) {
+            ptx::tc_fence_after();
+            const int tok_g = tok0 + t * R + tok_l;
+            const bool store = row_valid && tok_g < a.total_tokens;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const long long orow = ((long long)tok_g * a.hq + (long long)g * G + jh);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                ptx::tc_ld32(tO + 32 * c, v);
+                ptx::tc_wait_ld();
+                if (store) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(a.o + orow * kHeadDim + 32 * c);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 w;
+                        w.x = ptx::pack_bf16(__uint_as_float(v[8 * q + 0]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
+                        w.y = ptx::pack_bf16(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
+                        w.z = ptx::pack_bf16(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
+                        w.w = ptx::pack_bf16(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
+                        dst[q] = w;
+                    }
+                }
+            }
+            if (store) {
+                a.lse[orow] = (m_ref + log2f(l)) * kLn2;
+                if (a.positions && jh == 0 && __ldg(a.positions + tok_g) != limit)
+                    report(a.status, MSGL_DEVERR_POSITION);
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp >= 4) {
+        // rows that would have read a key behind a bad page id: o = 0, lse = -inf
+        const int bad_key = *min_bad;
+        if (bad_key != INT_MAX) {
+            const int t = (warp - 4) >> 2;
+            const int r = (warp & 3) * 32 + lane;
+            const int tok_l = r / G, jh = r - tok_l * G;
+            const int n_t = t == 0 ? nA : nB;
+            const int tok_g = tok0 + t * R + tok_l;
+            if (r < R * G && tok_l < n_t && tok_g < a.total_tokens && pre + i0 + t * R + tok_l >= bad_key) {
+                const long long orow = ((long long)tok_g * a.hq + (long long)g * G + jh);
+                uint4 *dst = reinterpret_cast<uint4 *>(a.o + orow * kHeadDim);
+                for (int q = 0; q < 16; ++q) dst[q] = make_uint4(0, 0, 0, 0);
+                a.lse[orow] = -INFINITY;
+            }
+            if (threadIdx.x == 128) report(a.status, MSGL_DEVERR_PAGE_RANGE);
+        }
+    }
+    if (warp == 2) {
+        ptx::tc_fence_after();
+        ptx::tc_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+}  // namespace
+
+size_t extend_workspace_bytes(int32_t, int32_t, int32_t, int32_t, int32_t) { return 0; }
 
 cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t stream) {
     if (a.num_reqs == 0 || a.total_tokens == 0 || a.max_ext_len == 0) return cudaSuccess;
-    RowsArgs r{};
-    r.pool = a.pool;
-    r.pages = a.pages;
-    r.q = a.q;
-    r.hq = a.hq;
-    r.total_tokens = a.total_tokens;
-    r.scale_log2 = a.scale * kLog2e;
-    r.max_seq_len = a.max_seq_len;
-    r.prefix_lens = a.prefix_lens;
-    r.ext_lens = a.ext_lens;
-    r.cu_ext = a.cu_ext;
-    r.positions = a.positions;
-    r.chunk = a.max_seq_len;
-    r.num_splits = 1;
-    r.o = a.o;
-    r.lse = a.lse;
-    r.status = a.status;
-    const int G = a.hq / a.pool.hkv;
-    dim3 grid(a.max_ext_len, a.pool.hkv, a.num_reqs);
-    switch (G) {
-        case 1: launch_rows_extend<1>(r, grid, stream); break;
-        case 2: launch_rows_extend<2>(r, grid, stream); break;
-        case 3: launch_rows_extend<3>(r, grid, stream); break;
-        case 4: launch_rows_extend<4>(r, grid, stream); break;
-        case 5: launch_rows_extend<5>(r, grid, stream); break;
-        case 6: launch_rows_extend<6>(r, grid, stream); break;
-        case 7: launch_rows_extend<7>(r, grid, stream); break;
-        case 8: launch_rows_extend<8>(r, grid, stream); break;
-        default: return cudaErrorInvalidValue;
+    const int hkv = a.pool.hkv;
+    const int G = a.hq / hkv;
+    const int R = kRows / G;
+    const int q_box_rows = R < a.total_tokens ? R : a.total_tokens;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+
+    CUtensorMap qm, km, vm;
+    {
+        cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)a.hq, (cuuint64_t)a.total_tokens};
+        cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)a.hq * kHeadDim * 2};
+        cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)q_box_rows};
+        cuuint32_t es[3] = {1, 1, 1};
+        if (enc(&qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void *)a.q, dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
     }
+    const long long pool_rows = a.pool.num_slots * hkv;
+    if (pool_rows >= INT_MAX) return cudaErrorInvalidValue;
+    // 2D view {128 dims, slots x heads} for four-row gathers
+    for (int which = 0; which < 2; ++which) {
+        cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)pool_rows};
+        cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+        cuuint32_t box[2] = {64, 1};
+        cuuint32_t es[2] = {1, 1};
+        if (enc(which ? &vm : &km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                (void *)(which ? a.pool.v : a.pool.k), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    // tiled 3D view {128 dims, Hkv heads, slots}: one box = box_rows slots of one head
+    CUtensorMap ktm, vtm;
+    memset(&ktm, 0, sizeof ktm);
+    memset(&vtm, 0, sizeof vtm);
+    const int page = 1 << a.pool.log2_ps;
+    const int box_rows = page >= 16 ? (page < kKeys ? page : kKeys) : 0;
+    for (int which = 0; box_rows > 0 && which < 2; ++which) {
+        cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv, (cuuint64_t)a.pool.num_slots};
+        cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)hkv * kHeadDim * 2};
+        cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+        cuuint32_t es[3] = {1, 1, 1};
+        if (enc(which ? &vtm : &ktm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                (void *)(which ? a.pool.v : a.pool.k), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    static bool attr_set[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(extend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    ExtendKernelArgs k{};
+    k.pool = a.pool;
+    k.pages = a.pages;
+    k.prefix_lens = a.prefix_lens;
+    k.ext_lens = a.ext_lens;
+    k.cu_ext = a.cu_ext;
+    k.positions = a.positions;
+    k.hq = a.hq;
+    k.group = G;
+    k.rows_per_tile = R;
+    k.q_box_rows = q_box_rows;
+    k.total_tokens = a.total_tokens;
+    k.num_reqs = a.num_reqs;
+    k.nblk = (a.max_ext_len + 2 * R - 1) / (2 * R);
+    k.oob_row = (int)pool_rows;
+    k.box_rows = box_rows;
+    k.scale_log2 = a.scale * kLog2e;
+    k.o = a.o;
+    k.lse = a.lse;
+    k.status = a.status;
+    const long long grid = (long long)k.nblk * hkv * a.num_reqs;
+    if (grid >= INT_MAX) return cudaErrorInvalidValue;
+    extend_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(qm, km, vm, ktm, vtm, k);
     return cudaGetLastError();
 }
 
