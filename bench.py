@@ -166,6 +166,24 @@ def dist_info():
     return ws, rank, local
 
 
+def aggregate_over_ranks(work: dict, times: dict, ws: int, device=None) -> dict:
+    """Sum the per-rank work and take the max over ranks of each time (torch.distributed).
+
+    Each rank runs its own replica of the step on its own GPU, so there is no data-path
+    exchange: only these few scalars cross ranks, after the timed region.
+    """
+    if ws <= 1:
+        return {**work, **times}
+    import torch
+    import torch.distributed as dist
+    wk, tk = sorted(work), sorted(times)
+    w = torch.tensor([float(work[k]) for k in wk], dtype=torch.float64, device=device)
+    t = torch.tensor([float(times[k]) for k in tk], dtype=torch.float64, device=device)
+    dist.all_reduce(w, op=dist.ReduceOp.SUM)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return {**dict(zip(wk, w.tolist())), **dict(zip(tk, t.tolist()))}
+
+
 # --------------------------------------------------------- oracle timing
 
 def oracle_sample(w, cpu_seconds, n_threads):
@@ -348,16 +366,15 @@ def run_ours(args):
     mean = statistics.mean
     dec_bytes, ext_flops, st_bytes = A.decode_kv_bytes(w), A.extend_flops(w), A.store_bytes(w)
 
-    if ws > 1:
-        t = torch.tensor([total_ms, mean(dec_ms), mean(ext_ms)], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms, dec_avg, ext_avg = t.tolist()
-    else:
-        dec_avg, ext_avg = mean(dec_ms), mean(ext_ms)
+    job = aggregate_over_ranks({"decode_bytes": dec_bytes, "extend_flops": ext_flops},
+                               {"total_ms": total_ms, "decode_ms": mean(dec_ms), "extend_ms": mean(ext_ms)},
+                               ws, dev)
+    total_ms, dec_avg, ext_avg = job["total_ms"], job["decode_ms"], job["extend_ms"]
     st_avg = mean(store_ms)
     peaks = load_peaks()
-    dec_gbs = ws * dec_bytes / (dec_avg * 1e-3) / 1e9 if d is not None else None
-    ext_tf = ws * ext_flops / (ext_avg * 1e-3) / 1e12 if e is not None else None
+    # whole-job throughput: work summed over the replicas / the slowest replica's time
+    dec_gbs = job["decode_bytes"] / (dec_avg * 1e-3) / 1e9 if d is not None else None
+    ext_tf = job["extend_flops"] / (ext_avg * 1e-3) / 1e12 if e is not None else None
     st_gbs = st_bytes / (st_avg * 1e-3) / 1e9 if st_avg > 0 else None
 
     per_gpu_dec = dec_bytes / (dec_avg * 1e-3) / 1e9 if d is not None else None
