@@ -242,38 +242,62 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_o = ptx::umma_idesc_bf16(128, 128, false, true);
             bool ok = wait_or_abort(bar(kQFull), 0, abort_flag, a.status);
             ptx::tc_fence_after();
+            // S_t = Q_t K_j^T for tile t (8 MMAs over the 128 dims)
+            auto issue_s = [&](int t, int j) {
+                const uint32_t kb = sbase + kOffK + (j & 1) * kTile;
+                const uint32_t qb = sbase + kOffQ + t * kTile;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    ptx::tc_mma_ss(tmem + 128 * t, ptx::umma_desc_sw128(qb + off, 16, 1024),
+                                   ptx::umma_desc_sw128(kb + off, 16, 1024), idesc_s, kk > 0);
+                }
+                ptx::tc_commit(bar(kSFull + t));
+            };
+            // O_t += P_t V_j (P from TMEM, 8 MMAs over the 128 keys)
+            auto issue_pv = [&](int t, int j) {
+                const uint32_t vb = sbase + kOffV + (j & 1) * kTile;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    ptx::tc_mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8,
+                                   ptx::umma_desc_sw128(vb + kk * 2048, kHalf, 1024), idesc_o,
+                                   (j > 0 || kk > 0) ? 1u : 0u);
+                ptx::tc_commit(bar(kOFull + t));
+            };
+            // Order per K/V tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).  The next S of a
+            // tile goes in right after its PV (same TMEM columns; tcgen05 MMAs from one
+            // thread execute in order), so tile 0's next softmax overlaps tile 1's.
+            if (ok && (ok = wait_or_abort(bar(kKFull + 0), 0, abort_flag, a.status))) {
+                ptx::tc_fence_after();
+                if (nkv0 > 0) issue_s(0, 0);
+                if (nkv1 > 0) issue_s(1, 0);
+                ptx::tc_commit(bar(kKEmpty + 0));
+            }
             for (int j = 0; ok && j < nkv; ++j) {
                 const int s = j & 1, ph = (j >> 1) & 1;
-                if (!(ok = wait_or_abort(bar(kKFull + s), ph, abort_flag, a.status))) break;
-                ptx::tc_fence_after();
-                const uint32_t kb = sbase + kOffK + s * kTile;
-                for (int t = 0; t < 2; ++t) {
-                    if (j >= (t ? nkv1 : nkv0)) continue;
-                    const uint32_t qb = sbase + kOffQ + t * kTile;
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                        ptx::tc_mma_ss(tmem + 128 * t, ptx::umma_desc_sw128(qb + off, 16, 1024),
-                                       ptx::umma_desc_sw128(kb + off, 16, 1024), idesc_s, kk > 0);
-                    }
-                    ptx::tc_commit(bar(kSFull + t));
-                }
-                ptx::tc_commit(bar(kKEmpty + s));
+                const int jn = j + 1, sn = jn & 1, phn = (jn >> 1) & 1;
                 if (!(ok = wait_or_abort(bar(kVFull + s), ph, abort_flag, a.status))) break;
                 ptx::tc_fence_after();
-                const uint32_t vb = sbase + kOffV + s * kTile;
-                for (int t = 0; t < 2; ++t) {
-                    if (j >= (t ? nkv1 : nkv0)) continue;
-                    if (!(ok = wait_or_abort(bar(kPFull + t), j & 1, abort_flag, a.status))) break;
+                if (j < nkv0) {
+                    if (!(ok = wait_or_abort(bar(kPFull + 0), j & 1, abort_flag, a.status))) break;
                     ptx::tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        ptx::tc_mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8,
-                                       ptx::umma_desc_sw128(vb + kk * 2048, kHalf, 1024), idesc_o,
-                                       (j > 0 || kk > 0) ? 1u : 0u);
-                    ptx::tc_commit(bar(kOFull + t));
+                    issue_pv(0, j);
                 }
-                if (!ok) break;
+                const bool more = jn < nkv;
+                if (more) {
+                    if (!(ok = wait_or_abort(bar(kKFull + sn), phn, abort_flag, a.status))) break;
+                    ptx::tc_fence_after();
+                    if (jn < nkv0) issue_s(0, jn);
+                }
+                if (j < nkv1) {
+                    if (!(ok = wait_or_abort(bar(kPFull + 1), j & 1, abort_flag, a.status))) break;
+                    ptx::tc_fence_after();
+                    issue_pv(1, j);
+                }
+                if (more) {
+                    if (jn < nkv1) issue_s(1, jn);
+                    ptx::tc_commit(bar(kKEmpty + sn));
+                }
                 ptx::tc_commit(bar(kVEmpty + s));
             }
             // drain: every MMA issued above has completed once this fires
@@ -303,66 +327,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             const bool masked = j >= jm;             // uniform: only tiles past the first row's limit
             const int lim = limit - j * kKeys;       // key c of this tile is visible iff c <= lim
-            // pass 1: row max of the raw scores
+            // one TMEM read of the row's 128 scores
+            uint32_t v[128];
+            ptx::tc_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(v + 0));
+            ptx::tc_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+            ptx::tc_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
+            ptx::tc_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
+            ptx::tc_wait_ld();
+            if (masked) {
+#pragma unroll
+                for (int i = 0; i < 128; ++i)
+                    if (i > lim) v[i] = __float_as_uint(-INFINITY);
+            }
             float mxa = -INFINITY, mxb = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                ptx::tc_ld32(tS + 32 * c, v);
-                ptx::tc_wait_ld();
-                if (!masked) {
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        mxa = ptx::max3(mxa, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-                        mxb = ptx::max3(mxb, __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const float x0 = (32 * c + i <= lim) ? __uint_as_float(v[i]) : -INFINITY;
-                        const float x1 = (32 * c + i + 1 <= lim) ? __uint_as_float(v[i + 1]) : -INFINITY;
-                        mxa = ptx::max3(mxa, x0, x1);
-                    }
-                }
+            for (int i = 0; i < 128; i += 4) {
+                mxa = ptx::max3(mxa, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                mxb = ptx::max3(mxb, __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
             }
             const float m_new = fmaxf(m_ref, fmaxf(mxa, mxb) * a.scale_log2);
             const bool need = m_new > m_ref + 8.f;
             if (j > 0 && __any_sync(0xffffffffu, need)) {
                 const float alpha = need ? ptx::ex2(m_ref - m_new) : 1.f;
-#pragma unroll
+#pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
-                    uint32_t v[32];
-                    ptx::tc_ld32(tO + 32 * c, v);
+                    uint32_t o32[32];
+                    ptx::tc_ld32(tO + 32 * c, o32);
                     ptx::tc_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-                    ptx::tc_st32(tO + 32 * c, v);
+                    for (int i = 0; i < 32; ++i) o32[i] = __float_as_uint(__uint_as_float(o32[i]) * alpha);
+                    ptx::tc_st32(tO + 32 * c, o32);
                 }
                 ptx::tc_wait_st();
                 l *= alpha;
             }
             if (need) m_ref = m_new;
-            // pass 2: P = 2^(s * scale_log2 - m_ref), written back over S as bf16 pairs
+            // P = 2^(s * scale_log2 - m_ref) (masked scores are -inf -> 0), back over S as bf16
             const uint64_t sc2 = ptx::f2_pack(a.scale_log2, a.scale_log2);
             const uint64_t nm2 = ptx::f2_pack(-m_ref, -m_ref);
             uint64_t l2 = ptx::f2_pack(0.f, 0.f);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                ptx::tc_ld32(tS + 32 * c, v);
-                ptx::tc_wait_ld();
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const uint64_t x2 = ptx::f2_fma(
-                        ptx::f2_pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), sc2, nm2);
+                    const int e = 32 * c + 2 * i;
+                    const uint64_t x2 = ptx::f2_fma(ptx::f2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                                    sc2, nm2);
                     float x0, x1;
                     ptx::f2_unpack(x2, x0, x1);
-                    float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
-                    if (masked) {
-                        p0 = (32 * c + 2 * i <= lim) ? p0 : 0.f;
-                        p1 = (32 * c + 2 * i + 1 <= lim) ? p1 : 0.f;
-                    }
+                    const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
                     l2 = ptx::f2_add(l2, ptx::f2_pack(p0, p1));
                     pk[i] = ptx::pack_bf16(p0, p1);
                 }
