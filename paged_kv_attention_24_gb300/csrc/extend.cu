@@ -13,7 +13,7 @@
 //   loaded by one 3D TMA box per 64-dim half straight from q[T, Hq, 128].
 //   Every K/V byte staged in shared memory feeds all G heads.
 // * A CTA owns two such tiles (2R tokens) of one request and one kv head and
-//   streams 128-key K and V tiles through a 2-stage ring.  A page that is a
+//   streams 128-key K and V tiles through 2-stage (K) and 3-stage (V) rings.  A page that is a
 //   contiguous, fully valid run of pool rows (page_size >= 16) arrives in one
 //   tiled TMA box per 64-dim half; any other keys are gathered four pool
 //   rows per copy (TMA gather4).  A key beyond the causal range, or behind a
@@ -46,19 +46,20 @@ namespace {
 
 constexpr int kRows = 128;                 // rows per Q tile (MMA M)
 constexpr int kKeys = 128;                 // keys per K/V tile (MMA N of S, K of PV)
-constexpr int kStages = 2;
+constexpr int kStages = 2;                 // K tiles in flight
+constexpr int kVStages = 3;                // V tiles in flight (V is needed later than K)
 constexpr int kThreads = 384;              // 12 warps
 constexpr uint32_t kHalf = 16384;          // 128 rows x 128 bytes (64 bf16)
 constexpr uint32_t kTile = 2 * kHalf;      // 128 x 128 bf16
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + 2 * kTile;
 constexpr uint32_t kOffV = kOffK + kStages * kTile;
-constexpr uint32_t kOffBar = kOffV + kStages * kTile;
+constexpr uint32_t kOffBar = kOffV + kVStages * kTile;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // + slack to align the base to 1024
 
 // barrier slots
-constexpr int kQFull = 0, kKFull = 1, kKEmpty = 3, kVFull = 5, kVEmpty = 7, kSFull = 9, kPFull = 11,
-              kOFull = 13, kDrain = 15, kNumBars = 16;
+constexpr int kQFull = 0, kKFull = 1, kKEmpty = 3, kVFull = 5, kVEmpty = 8, kSFull = 11, kPFull = 13,
+              kOFull = 15, kDrain = 17, kNumBars = 18;
 
 struct ExtendKernelArgs {
     PoolView pool;
@@ -128,6 +129,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(bar(kKFull + s), 1);
             ptx::mbar_init(bar(kKEmpty + s), 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
             ptx::mbar_init(bar(kVFull + s), 1);
             ptx::mbar_init(bar(kVEmpty + s), 1);
         }
@@ -221,18 +224,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) ptx::mbar_arrive_expect_tx(bar(kKFull + s), kTile);
             __syncwarp();
             issue(sbase + kOffK + s * kTile + lane * 512, &k_map, &kt_map, bar(kKFull + s));
-            if (!wait_or_abort(bar(kVEmpty + s), (rnd & 1) ^ 1, abort_flag, a.status)) { issued = j + 1; break; }
-            if (lane == 0) ptx::mbar_arrive_expect_tx(bar(kVFull + s), kTile);
+            const int sv = j % kVStages, rv = j / kVStages;
+            if (!wait_or_abort(bar(kVEmpty + sv), (rv & 1) ^ 1, abort_flag, a.status)) { issued = j + 1; break; }
+            if (lane == 0) ptx::mbar_arrive_expect_tx(bar(kVFull + sv), kTile);
             __syncwarp();
-            issue(sbase + kOffV + s * kTile + lane * 512, &v_map, &vt_map, bar(kVFull + s));
+            issue(sbase + kOffV + sv * kTile + lane * 512, &v_map, &vt_map, bar(kVFull + sv));
             issued = j + 1;
         }
         if (*abort_flag) {
             // let issued copies land before shared memory goes away (bounded waits)
             ptx::mbar_wait(bar(kQFull), 0, 200000000LL);
-            for (int j = max(0, issued - kStages); j < issued; ++j) {
-                ptx::mbar_wait(bar(kKFull + (j & 1)), (j >> 1) & 1, 200000000LL);
-                ptx::mbar_wait(bar(kVFull + (j & 1)), (j >> 1) & 1, 200000000LL);
+            for (int j = max(0, issued - kVStages); j < issued; ++j) {
+                if (j >= issued - kStages) ptx::mbar_wait(bar(kKFull + (j & 1)), (j >> 1) & 1, 200000000LL);
+                ptx::mbar_wait(bar(kVFull + (j % kVStages)), (j / kVStages) & 1, 200000000LL);
             }
         }
     } else if (warp == 1) {
@@ -256,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             // O_t += P_t V_j (P from TMEM, 8 MMAs over the 128 keys)
             auto issue_pv = [&](int t, int j) {
-                const uint32_t vb = sbase + kOffV + (j & 1) * kTile;
+                const uint32_t vb = sbase + kOffV + (j % kVStages) * kTile;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     ptx::tc_mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8,
@@ -274,9 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_commit(bar(kKEmpty + 0));
             }
             for (int j = 0; ok && j < nkv; ++j) {
-                const int s = j & 1, ph = (j >> 1) & 1;
                 const int jn = j + 1, sn = jn & 1, phn = (jn >> 1) & 1;
-                if (!(ok = wait_or_abort(bar(kVFull + s), ph, abort_flag, a.status))) break;
+                if (!(ok = wait_or_abort(bar(kVFull + j % kVStages), (j / kVStages) & 1, abort_flag, a.status))) break;
                 ptx::tc_fence_after();
                 if (j < nkv0) {
                     if (!(ok = wait_or_abort(bar(kPFull + 0), j & 1, abort_flag, a.status))) break;
@@ -298,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (jn < nkv1) issue_s(1, jn);
                     ptx::tc_commit(bar(kKEmpty + sn));
                 }
-                ptx::tc_commit(bar(kVEmpty + s));
+                ptx::tc_commit(bar(kVEmpty + j % kVStages));
             }
             // drain: every MMA issued above has completed once this fires
             ptx::tc_commit(bar(kDrain));

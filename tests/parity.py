@@ -1,8 +1,14 @@
 """Shared parity helpers: GPU results against the fp64 oracle.
 
-Tolerances (bf16 inputs, fp32 accumulation, bf16 output): on O the max
-absolute error is at most 1e-2 and the mean absolute error at most 1e-3;
-on the natural-log LSE the max absolute error is at most 1e-3.
+Tolerances (bf16 inputs, fp32 accumulation, bf16 output).  On the five
+workloads the bar is the stated one: O max absolute error <= 1e-2, O mean
+absolute error <= 1e-3, LSE max absolute error <= 1e-3.
+
+Synthetic edge cases include rows that see only one to three keys, where
+|o| can reach 4 or more.  There, rounding o to bf16 alone can cost half a
+bf16 ulp, up to 2^-8 * |o| (0.0156 at |o| = 4), whatever the internal
+precision.  Those tests (``rounding_aware=True``) therefore allow, per
+element, 1e-2 + 2^-8 * |o_ref|, and keep the mean bound of 1e-3.
 """
 import numpy as np
 import torch
@@ -10,11 +16,15 @@ import torch
 O_MAX, O_MEAN, LSE_MAX = 1e-2, 1e-3, 1e-3
 
 
-def assert_o_close(o_gpu, o_ref, what=""):
+def assert_o_close(o_gpu, o_ref, what="", rounding_aware=False):
     o = o_gpu.double().cpu().numpy() if isinstance(o_gpu, torch.Tensor) else np.asarray(o_gpu, np.float64)
     assert np.isfinite(o).all(), f"{what}: non-finite output"
     err = np.abs(o - o_ref)
-    assert err.max() <= O_MAX, f"{what}: O max abs err {err.max():.3e} at {np.unravel_index(err.argmax(), err.shape)}"
+    bound = O_MAX + (np.abs(o_ref) * 2.0 ** -8 if rounding_aware else 0.0)
+    excess = err - bound
+    assert excess.max() <= 0, (f"{what}: O abs err {err.flat[excess.argmax()]:.3e} above bound "
+                               f"{np.broadcast_to(bound, err.shape).flat[excess.argmax()]:.3e} at "
+                               f"{np.unravel_index(excess.argmax(), err.shape)}")
     assert err.mean() <= O_MEAN, f"{what}: O mean abs err {err.mean():.3e}"
     return float(err.max()), float(err.mean())
 

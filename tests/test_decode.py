@@ -50,7 +50,7 @@ def test_decode_shapes(ps, hq, hkv):
     w = W.make_workload("shapes", hq, hkv, 128, ps, seed=ps * 100 + hq, decode_seq_lens=seqs, device="cuda")
     o, lse = run_gpu(w)
     ref_o, ref_l = run_oracle(w)
-    assert_o_close(o, ref_o, f"ps={ps} hq={hq} hkv={hkv}")
+    assert_o_close(o, ref_o, f"ps={ps} hq={hq} hkv={hkv}", rounding_aware=True)
     assert_lse_close(lse, ref_l)
 
 
@@ -59,7 +59,7 @@ def test_decode_long_single_request():
     w = W.make_workload("long", 16, 8, 128, 16, seed=3, decode_seq_lens=[65536], device="cuda")
     o, lse = run_gpu(w)
     ref_o, ref_l = run_oracle(w)
-    assert_o_close(o, ref_o)
+    assert_o_close(o, ref_o, rounding_aware=True)
     assert_lse_close(lse, ref_l)
 
 
@@ -69,7 +69,7 @@ def test_decode_uniform_values_and_large_scores():
     w.decode.q.mul_(4)
     o, lse = run_gpu(w)
     ref_o, ref_l = run_oracle(w)
-    assert_o_close(o, ref_o)
+    assert_o_close(o, ref_o, rounding_aware=True)
     assert_lse_close(lse, ref_l)
 
 
@@ -84,8 +84,8 @@ def test_decode_batch_equals_single():
         o1, l1 = ops.attn_decode(pool, d.q[b:b + 1].contiguous(), d.page_table[b:b + 1].contiguous(),
                                  d.seq_lens[b:b + 1].contiguous(), int(d.seq_lens[b]), w.scale)
         ref_o, ref_l = run_oracle(w, rows=[b])
-        assert_o_close(o1, ref_o)
-        assert_o_close(o[b:b + 1], ref_o)
+        assert_o_close(o1, ref_o, rounding_aware=True)
+        assert_o_close(o[b:b + 1], ref_o, rounding_aware=True)
 
 
 def test_decode_graph_capture_replay():
@@ -110,11 +110,11 @@ def test_decode_graph_capture_replay():
     graph.replay()
     torch.cuda.synchronize()
     ref_o, ref_l = run_oracle(w)
-    assert_o_close(o, ref_o)
+    assert_o_close(o, ref_o, rounding_aware=True)
     # new lengths, same graph: the kernels read seq_lens from device memory
     d.seq_lens.copy_(torch.tensor([1000, 1, 512], dtype=torch.int32))
     graph.replay()
     torch.cuda.synchronize()
     ref_o, ref_l = run_oracle(w)
-    assert_o_close(o, ref_o)
+    assert_o_close(o, ref_o, rounding_aware=True)
     assert_lse_close(lse, ref_l)

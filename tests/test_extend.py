@@ -94,7 +94,7 @@ def test_extend_ragged_shapes(ps, hq, hkv):
                         extend_ext_lens=ext, device="cuda")
     o, lse = run_gpu(w)
     ref_o, ref_l = run_oracle(w)
-    assert_o_close(o, ref_o, f"ps={ps} hq={hq}")
+    assert_o_close(o, ref_o, f"ps={ps} hq={hq}", rounding_aware=True)
     assert_lse_close(lse, ref_l)
 
 
@@ -104,7 +104,7 @@ def test_extend_shared_prefix_pages():
                         extend_ext_lens=[200, 64, 1, 333], shared_prefix_len=512, device="cuda")
     o, lse = run_gpu(w)
     ref_o, ref_l = run_oracle(w)
-    assert_o_close(o, ref_o)
+    assert_o_close(o, ref_o, rounding_aware=True)
     assert_lse_close(lse, ref_l)
 
 
@@ -124,7 +124,7 @@ def test_chunked_equals_unchunked_on_gpu():
         assert (o.float() - o_full[lo:hi].float()).abs().max().item() <= 1e-2
         assert (l - l_full[lo:hi]).abs().max().item() <= 1e-3
     ref_o, ref_l = run_oracle(w)
-    assert_o_close(o_full, ref_o)
+    assert_o_close(o_full, ref_o, rounding_aware=True)
 
 
 def test_decode_equals_last_extend_row():
@@ -148,5 +148,90 @@ def test_extend_without_positions():
     o, lse = ops.attn_extend(pool, e.q, e.page_table, e.prefix_lens, e.ext_lens, e.cu_ext,
                              e.max_ext_len, e.max_seq_len, w.scale, positions=None)
     ref_o, ref_l = run_oracle(w)
-    assert_o_close(o, ref_o)
+    assert_o_close(o, ref_o, rounding_aware=True)
+    assert_lse_close(lse, ref_l)
+
+
+@pytest.mark.parametrize("ps", [2, 4, 8, 32, 128])
+@pytest.mark.parametrize("hq,hkv", [(24, 8), (48, 8), (56, 8), (12, 4)])
+def test_extend_group_and_page_variants(ps, hq, hkv):
+    """G = 3, 6, 7 (GQA padding rows in every Q tile) with gathered and tiled page paths."""
+    pre = [0, 129, 63, 300]
+    ext = [5, 250, 77, 131]
+    w = W.make_workload("variants", hq, hkv, 128, ps, seed=ps * 7 + hq, extend_prefix_lens=pre,
+                        extend_ext_lens=ext, device="cuda")
+    status = ops.new_status()
+    o, lse = run_gpu(w, status)
+    assert ops.read_status(status) == 0
+    ref_o, ref_l = run_oracle(w)
+    assert_o_close(o, ref_o, f"ps={ps} hq={hq}", rounding_aware=True)
+    assert_lse_close(lse, ref_l)
+
+
+@pytest.mark.parametrize("ext", [1, 2, 3, 7])
+def test_extend_chunk_smaller_than_tile(ext):
+    """Fewer tokens than one Q tile holds (the TMA box is clipped to the tokens that exist)."""
+    w = W.make_workload("tiny", 16, 8, 128, 16, seed=40 + ext, extend_prefix_lens=[37],
+                        extend_ext_lens=[ext], device="cuda")
+    o, lse = run_gpu(w)
+    ref_o, ref_l = run_oracle(w)
+    assert_o_close(o, ref_o, rounding_aware=True)
+    assert_lse_close(lse, ref_l)
+
+
+def test_extend_long_prefix_many_tiles():
+    """A 16k-token cached prefix with a short chunk: many K/V tiles, ring wrap-around."""
+    w = W.make_workload("longpre", 64, 8, 128, 64, seed=50, extend_prefix_lens=[16384, 3],
+                        extend_ext_lens=[40, 200], device="cuda")
+    o, lse = run_gpu(w)
+    ref_o, ref_l = run_oracle(w)
+    assert_o_close(o, ref_o, rounding_aware=True)
+    assert_lse_close(lse, ref_l)
+
+
+def test_extend_bad_page_zeroes_affected_rows():
+    """A page id past the pool: status bit set; rows that would read it are zero, earlier rows exact."""
+    ps = 16
+    w = W.make_workload("badpage", 16, 8, 128, ps, seed=51, extend_prefix_lens=[64], extend_ext_lens=[100],
+                        device="cuda")
+    e = w.extend
+    good_o, good_l = run_gpu(w)
+    pt = e.page_table.clone()
+    bad_page_idx = 7                                   # keys 112..127 -> chunk rows i >= 48
+    pt[0, bad_page_idx] = w.num_slots // ps + 3
+    pool = ops.KVPool(w.k_pool, w.v_pool, ps)
+    status = ops.new_status()
+    o, lse = ops.attn_extend(pool, e.q, pt, e.prefix_lens, e.ext_lens, e.cu_ext, e.max_ext_len,
+                             e.max_seq_len, w.scale, positions=e.positions, status=status)
+    assert ops.read_status(status) & ops.DEVERR_PAGE_RANGE
+    first_bad_row = bad_page_idx * ps - 64
+    assert torch.all(o[first_bad_row:] == 0)
+    assert torch.all(lse[first_bad_row:] == float("-inf"))
+    assert torch.equal(o[:first_bad_row], good_o[:first_bad_row])
+
+
+def test_extend_zero_length_requests_and_graph_replay():
+    """Requests with no chunk tokens write nothing; a captured extend replays with new inputs."""
+    w = W.make_workload("zero", 40, 8, 128, 16, seed=52, extend_prefix_lens=[10, 500, 0],
+                        extend_ext_lens=[0, 70, 33], device="cuda")
+    e = w.extend
+    pool = ops.KVPool(w.k_pool, w.v_pool, w.page_size)
+    o = torch.empty_like(e.q)
+    lse = torch.empty(e.q.shape[:2], dtype=torch.float32, device="cuda")
+    args = (pool, e.q, e.page_table, e.prefix_lens, e.ext_lens, e.cu_ext, e.max_ext_len, e.max_seq_len,
+            w.scale)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        ops.attn_extend(*args, out=o, lse=lse)
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        ops.attn_extend(*args, out=o, lse=lse)
+    e.q.copy_(torch.randn_like(e.q.float()).to(torch.bfloat16))
+    o.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    ref_o, ref_l = run_oracle(w)
+    assert_o_close(o, ref_o, rounding_aware=True)
     assert_lse_close(lse, ref_l)
