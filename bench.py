@@ -48,6 +48,7 @@ def parse_args(argv=None):
     ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="approximate CPU seconds for the oracle sample")
     return ap.parse_args(argv)
@@ -402,6 +403,29 @@ def run_ours(args):
     if not args.no_e2e:
         e2e = measure_e2e(args, w, pool, k_new, v_new, loc, dev, dec_bytes, ext_flops)
 
+    append = None
+    if d is not None:
+        # the decode batch through msgl_attn_decode_append (current-token K/V stored in the same launch)
+        dk, dv = w.k_pool[d.new_loc.long()].contiguous(), w.v_pool[d.new_loc.long()].contiguous()
+        for _ in range(3):
+            ops.attn_decode_append(pool, d.q, dk, dv, d.new_loc, d.page_table, d.seq_lens, d.max_seq_len,
+                                   w.scale, out=o_d, lse=l_d, workspace=ws_d, status=status)
+        n_app = 50
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n_app):
+            ops.attn_decode_append(pool, d.q, dk, dv, d.new_loc, d.page_table, d.seq_lens, d.max_seq_len,
+                                   w.scale, out=o_d, lse=l_d, workspace=ws_d, status=status)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        app_ms = a0.elapsed_time(a1) / n_app
+        append = {"value": dec_bytes / (app_ms * 1e-3) / 1e9, "unit": "GB/s", "us_per_call": app_ms * 1e3,
+                  "note": "decode with the current token's K/V stored in the same launch"}
+
+    graph = None
+    if not args.no_graph:
+        graph = measure_graph(args, step, stream, total_ms / args.steps, dev)
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         import oracle
@@ -433,12 +457,84 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
+        "graph": graph,
+        "decode_append": append,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def measure_graph(args, step, stream, eager_ms, dev):
+    """The same step captured once in a CUDA graph and replayed (what a serving loop does).
+
+    Also times a 4-request decode (16/8 heads, lengths 17-200) eagerly and as a graph
+    replay, where launch overhead is a visible share of the call.
+    """
+    import torch
+    from paged_kv_attention_24_gb300 import ops
+    from paged_kv_attention_24_gb300 import workloads as W
+    reps = max(20, min(args.steps, 200))
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()
+    stream.wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    step_ms = t0.elapsed_time(t1) / reps
+
+    w = W.config(1, device=dev, part="decode")
+    d = w.decode
+    pool = ops.KVPool(w.k_pool, w.v_pool, w.page_size)
+    o = torch.empty_like(d.q)
+    l = torch.empty(d.q.shape[:2], dtype=torch.float32, device=dev)
+    ws = torch.empty(ops.decode_workspace_size(d.num_reqs, w.hq, w.hkv, d.max_seq_len), dtype=torch.uint8,
+                     device=dev)
+
+    def small():
+        ops.attn_decode(pool, d.q, d.page_table, d.seq_lens, d.max_seq_len, w.scale, out=o, lse=l, workspace=ws)
+
+    for _ in range(5):
+        small()
+    torch.cuda.synchronize()
+    n = 500
+    t0.record(stream)
+    for _ in range(n):
+        small()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    small_eager_us = 1e3 * t0.elapsed_time(t1) / n
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        small()
+    stream.wait_stream(side)
+    gs = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gs):
+        small()
+    gs.replay()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(n):
+        gs.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    small_graph_us = 1e3 * t0.elapsed_time(t1) / n
+    return {"ms_per_step": step_ms, "eager_ms_per_step": eager_ms, "replays": reps,
+            "small_decode_us": {"workload": W.CONFIG_NAMES[1], "eager": small_eager_us,
+                                "graph": small_graph_us}}
 
 
 def measure_e2e(args, w, pool, k_new, v_new, loc, dev, dec_bytes, ext_flops):

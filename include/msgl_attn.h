@@ -75,6 +75,7 @@ typedef enum msgl_status {
 #define MSGL_DEVERR_LENGTH 0x4u      /* decode seq_len < 1, or lengths inconsistent with cu_ext */
 #define MSGL_DEVERR_POSITION 0x8u    /* positions[t] != prefix_len + i for chunk row i */
 #define MSGL_DEVERR_TIMEOUT 0x10u    /* a bounded in-kernel wait gave up */
+#define MSGL_DEVERR_APPEND_SLOT 0x20u /* decode_append: new_loc[b] is not the slot of key seq_lens[b]-1 */
 
 /*
  * The unified KV pool of one layer.  k_pool and v_pool are device bf16
@@ -180,6 +181,31 @@ MSGL_API msgl_status msgl_attn_decode(const msgl_kv_pool *pool, const msgl_page_
                              int32_t num_reqs, int32_t max_seq_len, float scale, void *o,
                              float *lse, void *workspace, size_t workspace_bytes,
                              uint32_t *status, msgl_stream_t stream);
+
+/*
+ * Decode with the current token appended in the same launch: msgl_store_kv of
+ * each request's new K/V row followed by msgl_attn_decode, fused.  The K/V an
+ * attention call reads is the pool's history plus the newly computed K/V
+ * ("不懂SGLang？从miniSGLang开始", §1.3 item 1), and decode runs once per
+ * forward for every running request ("Mini-SGLang 实战指南", §6.3, §6.4).
+ *
+ *   k_new, v_new  device bf16 [num_reqs, num_kv_heads, head_dim]: the K/V of
+ *                 each request's current token (key seq_lens[b]-1)
+ *   new_loc       device int32 [num_reqs]: its pool slot, which must be the
+ *                 page-table slot of key seq_lens[b]-1 (else
+ *                 MSGL_DEVERR_APPEND_SLOT; an out-of-range slot sets
+ *                 MSGL_DEVERR_SLOT_RANGE and nothing is written)
+ * Every other argument, the outputs, the workspace and the status bits are
+ * those of msgl_attn_decode.  Key seq_lens[b]-1 is attended from k_new/v_new
+ * directly (it is not read back from the pool), and the row is written to
+ * the pool bit-exact during the same launch.
+ */
+MSGL_API msgl_status msgl_attn_decode_append(const msgl_kv_pool *pool, const msgl_page_table *pages,
+                                    const void *q, int32_t num_q_heads, const void *k_new,
+                                    const void *v_new, const int32_t *new_loc,
+                                    const int32_t *seq_lens, int32_t num_reqs, int32_t max_seq_len,
+                                    float scale, void *o, float *lse, void *workspace,
+                                    size_t workspace_bytes, uint32_t *status, msgl_stream_t stream);
 
 /*
  * Decode for callers that cannot allocate device memory.  It has no

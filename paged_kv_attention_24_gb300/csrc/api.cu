@@ -90,6 +90,54 @@ namespace msgl {
 void set_last_error(const char *msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
 }  // namespace msgl
 
+static msgl_status decode_impl(const msgl_kv_pool *pool, const msgl_page_table *pages, const void *q,
+                               int32_t num_q_heads, const void *k_new, const void *v_new,
+                               const int32_t *new_loc, const int32_t *seq_lens, int32_t num_reqs,
+                               int32_t max_seq_len, float scale, void *o, float *lse, void *workspace,
+                               size_t workspace_bytes, uint32_t *status, msgl_stream_t stream) {
+    g_last_error[0] = 0;
+    msgl::PoolView pv;
+    msgl::PageView pg;
+    msgl_status s = check_pool(pool, pv);
+    if (s) return s;
+    if ((s = check_heads(num_q_heads, pool->num_kv_heads))) return s;
+    if ((s = check_scale(scale))) return s;
+    if (num_reqs < 0) return fail(MSGL_ERR_INVALID_ARG, "num_reqs < 0");
+    if (num_reqs == 0) return MSGL_OK;
+    if ((s = check_pages(pages, num_reqs, pg))) return s;
+    if (max_seq_len <= 0) return fail(MSGL_ERR_INVALID_ARG, "max_seq_len must be > 0");
+    if (!q || !seq_lens || !o || !lse) return fail(MSGL_ERR_INVALID_ARG, "q, seq_lens, o and lse must be non-NULL");
+    if (!aligned16(q) || !aligned16(o)) return fail(MSGL_ERR_INVALID_ARG, "q and o must be 16-byte aligned");
+    if (pool->num_kv_heads > 8 && pool->num_kv_heads % 8 != 0)
+        return fail(MSGL_ERR_UNSUPPORTED, "decode needs num_kv_heads <= 8 or a multiple of 8");
+    const msgl::DecodePlan plan = msgl::plan_decode(num_reqs, num_q_heads, pool->num_kv_heads, max_seq_len);
+    if (!workspace || workspace_bytes < plan.workspace)
+        return fail(MSGL_ERR_WORKSPACE, "decode needs %zu workspace bytes, got %zu", plan.workspace,
+                    workspace ? workspace_bytes : (size_t)0);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(MSGL_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    msgl::DecodeArgs a{};
+    a.pool = pv;
+    a.pages = pg;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.seq_lens = seq_lens;
+    a.num_reqs = num_reqs;
+    a.hq = num_q_heads;
+    a.max_seq_len = max_seq_len;
+    a.scale = scale;
+    a.o = static_cast<__nv_bfloat16 *>(o);
+    a.lse = lse;
+    a.part_o = static_cast<float *>(workspace);
+    a.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.o_bytes);
+    a.status = status;
+    a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    a.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    a.new_loc = new_loc;
+    cudaError_t e = msgl::launch_decode(a, plan, (cudaStream_t)stream);
+    return e == cudaSuccess ? MSGL_OK : cuda_fail(e, "decode launch");
+}
+
+
 extern "C" {
 
 int32_t msgl_abi_version(void) { return MSGL_ABI_VERSION; }
@@ -141,43 +189,25 @@ msgl_status msgl_attn_decode(const msgl_kv_pool *pool, const msgl_page_table *pa
                              int32_t num_reqs, int32_t max_seq_len, float scale, void *o,
                              float *lse, void *workspace, size_t workspace_bytes,
                              uint32_t *status, msgl_stream_t stream) {
+    return decode_impl(pool, pages, q, num_q_heads, nullptr, nullptr, nullptr, seq_lens, num_reqs,
+                       max_seq_len, scale, o, lse, workspace, workspace_bytes, status, stream);
+}
+
+msgl_status msgl_attn_decode_append(const msgl_kv_pool *pool, const msgl_page_table *pages,
+                                    const void *q, int32_t num_q_heads, const void *k_new,
+                                    const void *v_new, const int32_t *new_loc,
+                                    const int32_t *seq_lens, int32_t num_reqs, int32_t max_seq_len,
+                                    float scale, void *o, float *lse, void *workspace,
+                                    size_t workspace_bytes, uint32_t *status, msgl_stream_t stream) {
     g_last_error[0] = 0;
-    msgl::PoolView pv;
-    msgl::PageView pg;
-    msgl_status s = check_pool(pool, pv);
-    if (s) return s;
-    if ((s = check_heads(num_q_heads, pool->num_kv_heads))) return s;
-    if ((s = check_scale(scale))) return s;
-    if (num_reqs < 0) return fail(MSGL_ERR_INVALID_ARG, "num_reqs < 0");
-    if (num_reqs == 0) return MSGL_OK;
-    if ((s = check_pages(pages, num_reqs, pg))) return s;
-    if (max_seq_len <= 0) return fail(MSGL_ERR_INVALID_ARG, "max_seq_len must be > 0");
-    if (!q || !seq_lens || !o || !lse) return fail(MSGL_ERR_INVALID_ARG, "q, seq_lens, o and lse must be non-NULL");
-    if (!aligned16(q) || !aligned16(o)) return fail(MSGL_ERR_INVALID_ARG, "q and o must be 16-byte aligned");
-    if (pool->num_kv_heads > 8 && pool->num_kv_heads % 8 != 0)
-        return fail(MSGL_ERR_UNSUPPORTED, "decode needs num_kv_heads <= 8 or a multiple of 8");
-    const msgl::DecodePlan plan = msgl::plan_decode(num_reqs, num_q_heads, pool->num_kv_heads, max_seq_len);
-    if (!workspace || workspace_bytes < plan.workspace)
-        return fail(MSGL_ERR_WORKSPACE, "decode needs %zu workspace bytes, got %zu", plan.workspace,
-                    workspace ? workspace_bytes : (size_t)0);
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-        return fail(MSGL_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-    msgl::DecodeArgs a{};
-    a.pool = pv;
-    a.pages = pg;
-    a.q = static_cast<const __nv_bfloat16 *>(q);
-    a.seq_lens = seq_lens;
-    a.num_reqs = num_reqs;
-    a.hq = num_q_heads;
-    a.max_seq_len = max_seq_len;
-    a.scale = scale;
-    a.o = static_cast<__nv_bfloat16 *>(o);
-    a.lse = lse;
-    a.part_o = static_cast<float *>(workspace);
-    a.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.o_bytes);
-    a.status = status;
-    cudaError_t e = msgl::launch_decode(a, plan, (cudaStream_t)stream);
-    return e == cudaSuccess ? MSGL_OK : cuda_fail(e, "decode launch");
+    if (num_reqs > 0) {
+        if (!k_new || !v_new || !new_loc)
+            return fail(MSGL_ERR_INVALID_ARG, "k_new, v_new and new_loc must be non-NULL");
+        if (!aligned16(k_new) || !aligned16(v_new))
+            return fail(MSGL_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+    }
+    return decode_impl(pool, pages, q, num_q_heads, k_new, v_new, new_loc, seq_lens, num_reqs,
+                       max_seq_len, scale, o, lse, workspace, workspace_bytes, status, stream);
 }
 
 size_t msgl_extend_workspace_size(int32_t num_reqs, int32_t total_tokens, int32_t num_q_heads,

@@ -62,6 +62,10 @@ struct DecodeKernelArgs {
     float *part_o;
     float *part_lse;
     uint32_t *status;
+    // append mode (all three non-NULL): key seq_b-1 comes from k_new/v_new[b] and is
+    // written to the pool at new_loc[b]
+    const __nv_bfloat16 *k_new, *v_new;
+    const int32_t *new_loc;
 };
 
 __device__ __forceinline__ int seq_valid(const int32_t *seq_lens, int b, int max_seq) {
@@ -183,12 +187,37 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
                             ptx::mbar_arrive_expect_tx(full_bar, __popc(mask) * row_bytes * 2);
                         }
                         __syncwarp();
+                        // append mode: this tile holds the request's current token
+                        const bool has_new = a.new_loc && t0 + n == sb;
+                        const bool is_new = has_new && lane == n - 1;
                         if (ok) {
                             uint8_t *kdst = smem + (size_t)stage * sbytes + lane * pitch;
                             uint8_t *vdst = kdst + kTileKeys * pitch;
                             const long long off = slot * slot_elems + (long long)g0 * kHeadDim;
-                            ptx::bulk_g2s(ptx::smem_u32(kdst), a.pool.k + off, row_bytes, full_bar);
-                            ptx::bulk_g2s(ptx::smem_u32(vdst), a.pool.v + off, row_bytes, full_bar);
+                            const long long noff = (long long)b * slot_elems + (long long)g0 * kHeadDim;
+                            ptx::bulk_g2s(ptx::smem_u32(kdst), is_new ? a.k_new + noff : a.pool.k + off,
+                                          row_bytes, full_bar);
+                            ptx::bulk_g2s(ptx::smem_u32(vdst), is_new ? a.v_new + noff : a.pool.v + off,
+                                          row_bytes, full_bar);
+                        }
+                        if (has_new) {
+                            // write the new K/V rows of this head group into the pool at new_loc[b];
+                            // only this CTA touches key seq_b-1 in this launch
+                            const long long loc = __ldg(a.new_loc + b);
+                            const long long page_slot = __shfl_sync(0xffffffffu, slot, n - 1);
+                            if (loc < 0 || loc >= a.pool.num_slots) {
+                                if (lane == 0) report(a.status, MSGL_DEVERR_SLOT_RANGE);
+                            } else {
+                                if (lane == 0 && loc != page_slot) report(a.status, MSGL_DEVERR_APPEND_SLOT);
+                                const long long src = (long long)b * slot_elems + (long long)g0 * kHeadDim;
+                                const long long dst = loc * slot_elems + (long long)g0 * kHeadDim;
+                                for (int c = lane; c < (int)row_bytes / 16; c += 32) {
+                                    const uint4 kv = ld_stream_16(a.k_new + src + 8 * c);
+                                    const uint4 vv = ld_stream_16(a.v_new + src + 8 * c);
+                                    *reinterpret_cast<uint4 *>(const_cast<__nv_bfloat16 *>(a.pool.k) + dst + 8 * c) = kv;
+                                    *reinterpret_cast<uint4 *>(const_cast<__nv_bfloat16 *>(a.pool.v) + dst + 8 * c) = vv;
+                                }
+                            }
                         }
                         ++it;
                     }
@@ -362,11 +391,18 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
 // Fold the partials of request b, q head h: weights exp(lse_i - max),
 // o = sum w_i o_i / sum w_i, lse = max + ln(sum w_i).  A NaN partial lse
 // marks a segment that hit a bad index: the row is written as o = 0, lse = -inf.
+// One warp per (request, q head).  The lanes first share out the partials (max,
+// weights and their sum by warp reductions, weights kept in shared memory), then
+// each lane owns 4 of the 128 dims and sums the weighted partial rows, four
+// partials at a time so their loads overlap.
+constexpr int kMergeMaxParts = kMaxDecodeCtas + 1;
+
 __global__ void __launch_bounds__(256) decode_merge_kernel(
     const int32_t *__restrict__ seq_lens, int32_t num_reqs, int32_t max_seq_len, int32_t hq,
     int32_t num_ctas, const float *__restrict__ part_o, const float *__restrict__ part_lse,
     __nv_bfloat16 *__restrict__ o, float *__restrict__ lse, uint32_t *status) {
     __shared__ long long s_start, s_total;
+    __shared__ float s_w[8][kMergeMaxParts];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.y;
     if (warp == 0) {
@@ -398,28 +434,58 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(
     }
     const long long per = (s_total + num_ctas - 1) / num_ctas;
     const int first = (int)(s_start / per);
-    const int last = (int)((s_start + sb - 1) / per);
+    const int count = (int)((s_start + sb - 1) / per) - first + 1;   // <= num_ctas
+    // max over the partial LSEs (NaN = failed segment)
     float M = -INFINITY;
     bool failed = false;
-    for (int i = first; i <= last; ++i) {
-        const float x = part_lse[(long long)(b + i) * hq + h];
+    for (int i = lane; i < count; i += 32) {
+        const float x = part_lse[(long long)(b + first + i) * hq + h];
         if (isnan(x)) failed = true;
         else M = fmaxf(M, x);
     }
-    float L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+    failed = __any_sync(0xffffffffu, failed);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
     if (!failed && M != -INFINITY) {
-        for (int i = first; i <= last; ++i) {
-            const long long pr = (long long)(b + i) * hq + h;
-            const float w = __expf(part_lse[pr] - M);
-            const float4 v = *reinterpret_cast<const float4 *>(part_o + pr * kHeadDim + lane * 4);
+        for (int i = lane; i < count; i += 32) {
+            const float x = part_lse[(long long)(b + first + i) * hq + h];
+            const float w = x == -INFINITY ? 0.f : __expf(x - M);
+            s_w[warp][i] = w;
             L += w;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    }
+    __syncwarp();
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const bool zero = failed || !(L > 0.f);
+    if (!zero) {
+        const float *base = part_o + ((long long)(b + first) * hq + h) * kHeadDim + lane * 4;
+        const long long stride = (long long)hq * kHeadDim;
+        int i = 0;
+        for (; i + 4 <= count; i += 4) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = *reinterpret_cast<const float4 *>(base + (i + u) * stride);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float w = s_w[warp][i + u];
+                acc[0] += w * v[u].x;
+                acc[1] += w * v[u].y;
+                acc[2] += w * v[u].z;
+                acc[3] += w * v[u].w;
+            }
+        }
+        for (; i < count; ++i) {
+            const float4 v = *reinterpret_cast<const float4 *>(base + i * stride);
+            const float w = s_w[warp][i];
             acc[0] += w * v.x;
             acc[1] += w * v.y;
             acc[2] += w * v.z;
             acc[3] += w * v.w;
         }
     }
-    const bool zero = failed || !(L > 0.f);
     const float inv = zero ? 0.f : 1.f / L;
     const uint32_t lo = ptx::pack_bf16(acc[0] * inv, acc[1] * inv);
     const uint32_t hi = ptx::pack_bf16(acc[2] * inv, acc[3] * inv);
@@ -497,6 +563,9 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     k.part_o = a.part_o;
     k.part_lse = a.part_lse;
     k.status = a.status;
+    k.k_new = a.k_new;
+    k.v_new = a.v_new;
+    k.new_loc = a.new_loc;
     (void)plan;
     if (L.smem > (size_t)kSmemBudget) return cudaErrorInvalidValue;
     dim3 grid(L.ctas, hkv / L.hg);

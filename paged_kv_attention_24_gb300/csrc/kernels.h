@@ -34,6 +34,8 @@ struct DecodeArgs {
     float *part_o;      // [num_reqs + max CTAs, hq, 128] segment partials
     float *part_lse;    // [num_reqs + max CTAs, hq]
     uint32_t *status;
+    const __nv_bfloat16 *k_new = nullptr, *v_new = nullptr;   // append mode (see msgl_attn_decode_append)
+    const int32_t *new_loc = nullptr;
 };
 cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream);
 

@@ -27,6 +27,7 @@ DEVERR_PAGE_RANGE = 0x2
 DEVERR_LENGTH = 0x4
 DEVERR_POSITION = 0x8
 DEVERR_TIMEOUT = 0x10
+DEVERR_APPEND_SLOT = 0x20
 
 
 class MsglError(RuntimeError):
@@ -61,6 +62,7 @@ SIGNATURES = {
                          ctypes.c_int),
     "msgl_decode_workspace_size": ([I32, I32, I32, I32, I32], SZ),
     "msgl_attn_decode": ([PP, PT, P, I32, P, I32, I32, F32, P, P, P, SZ, P, P], ctypes.c_int),
+    "msgl_attn_decode_append": ([PP, PT, P, I32, P, P, P, P, I32, I32, F32, P, P, P, SZ, P, P], ctypes.c_int),
     "msgl_attn_decode_noalloc": ([PP, PT, P, I32, P, I32, I32, F32, P, P, P, P], ctypes.c_int),
     "msgl_read_status": ([P, ctypes.POINTER(ctypes.c_uint32), P], ctypes.c_int),
     "msgl_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -223,6 +225,34 @@ def attn_extend(pool: KVPool, q: torch.Tensor, page_table: torch.Tensor, prefix_
         0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(status),
         _stream(stream))
     _check(rc, "msgl_attn_extend")
+    return out, lse
+
+
+def attn_decode_append(pool: KVPool, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                       new_loc: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor,
+                       max_seq_len: int, scale: float, out: Optional[torch.Tensor] = None,
+                       lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                       status: Optional[torch.Tensor] = None, stream=None):
+    """Store each request's current-token K/V at new_loc and decode, in one launch."""
+    _need(q, "q", torch.bfloat16)
+    _need(k_new, "k_new", torch.bfloat16)
+    _need(v_new, "v_new", torch.bfloat16)
+    _need(new_loc, "new_loc", torch.int32)
+    _need(seq_lens, "seq_lens", torch.int32)
+    B, hq, d = q.shape
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty(B, hq, dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(out, "out", torch.bfloat16)
+    _need(lse, "lse", torch.float32)
+    if workspace is None:
+        workspace = _workspace(decode_workspace_size(B, hq, pool.num_kv_heads, max_seq_len, d), q.device)
+    pc, pt = pool.c(), _pages(page_table)
+    rc = load().msgl_attn_decode_append(
+        ctypes.byref(pc), ctypes.byref(pt), _ptr(q), hq, _ptr(k_new), _ptr(v_new), _ptr(new_loc),
+        _ptr(seq_lens), B, int(max_seq_len), float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(status),
+        _stream(stream))
+    _check(rc, "msgl_attn_decode_append")
     return out, lse
 
 
