@@ -161,17 +161,28 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
                 if (end_b > pos) {
                     const int lo = (int)(pos - start_b);
                     const int hi = (int)(min(r1, end_b) - start_b);
+                    // page id of key `key` of request b (-1 when the page index is past the
+                    // table's width, which then reads as a bad page)
+                    auto load_pid = [&](int key) -> int {
+                        const int pidx = key >> a.pool.log2_ps;
+                        return pidx < a.pages.width ? __ldg(a.pages.ids + (int64_t)b * a.pages.stride + pidx) : -1;
+                    };
+                    // the page ids of the next tile are loaded one tile ahead, so the table
+                    // lookup overlaps the wait for a free stage
+                    int pid_cur = lane < min(kTileKeys, hi - lo) ? load_pid(lo + lane) : -1;
                     for (int t0 = lo; t0 < hi; t0 += kTileKeys) {
                         const int stage = it % S, round = it / S;
-                        if (*abort_flag || !stage_wait_empty(stage, round)) { aborted = true; break; }
                         const int n = min(kTileKeys, hi - t0);
+                        const int t1 = t0 + kTileKeys;
+                        const int pid_next = (t1 < hi && lane < min(kTileKeys, hi - t1)) ? load_pid(t1 + lane) : -1;
+                        if (*abort_flag || !stage_wait_empty(stage, round)) { aborted = true; break; }
                         bool ok = false;
                         int64_t slot = -1;
-                        if (lane < n) {
-                            bool bad = false;
-                            slot = slot_of(a.pool, a.pages, b, t0 + lane, bad);
-                            ok = !bad;
+                        if (lane < n && pid_cur >= 0 && pid_cur < a.pool.num_pages) {
+                            slot = ((int64_t)pid_cur << a.pool.log2_ps) + ((t0 + lane) & ((1 << a.pool.log2_ps) - 1));
+                            ok = true;
                         }
+                        pid_cur = pid_next;
                         const uint32_t mask = __ballot_sync(0xffffffffu, ok);
                         const uint32_t badm = __ballot_sync(0xffffffffu, lane < n && !ok);
                         const uint32_t full_bar = ptx::smem_u32(full + stage);
