@@ -102,6 +102,8 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g0 = blockIdx.y * hg;   // first kv head of this CTA
+    // let the merge kernel launch now; it waits for this grid before reading partials
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -443,6 +445,8 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(
         if (lane == 0) lse[row] = -INFINITY;
         return;
     }
+    // the split kernel's partials are complete and visible after this point
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long per = (s_total + num_ctas - 1) / num_ctas;
     const int first = (int)(s_start / per);
     const int count = (int)((s_start + sb - 1) / per) - first + 1;   // <= num_ctas
@@ -583,10 +587,21 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     decode_split_kernel<<<grid, 32 * (L.hg + 1), L.smem, stream>>>(k);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    dim3 mgrid((a.hq + 7) / 8, a.num_reqs);
-    decode_merge_kernel<<<mgrid, 256, 0, stream>>>(a.seq_lens, a.num_reqs, a.max_seq_len, a.hq, L.ctas,
-                                                   a.part_o, a.part_lse, a.o, a.lse, a.status);
-    return cudaGetLastError();
+    // programmatic dependent launch: the merge's launch and its seq_lens scan overlap the
+    // tail of the split kernel
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((a.hq + 7) / 8, a.num_reqs);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_merge_kernel, a.seq_lens, a.num_reqs, a.max_seq_len, a.hq,
+                              L.ctas, (const float *)a.part_o, (const float *)a.part_lse, a.o, a.lse,
+                              a.status);
 }
 
 }  // namespace msgl
