@@ -243,6 +243,17 @@ MSGL_API msgl_status msgl_attn_decode_noalloc(const msgl_kv_pool *pool, const ms
  */
 MSGL_API msgl_status msgl_read_status(const uint32_t *status, uint32_t *flags, msgl_stream_t stream);
 
+/*
+ * Self-test of the bounded wait every kernel uses (no counterpart on the
+ * pages).  Launches one thread that waits on an mbarrier that nothing arrives
+ * at, with a budget of budget_cycles SM clocks (0 < budget <= 4e9; ~1e7 is
+ * about 5 ms).  The wait gives up, MSGL_DEVERR_TIMEOUT is ORed into *status,
+ * and the kernel returns normally.  Use it to check that a lost arrival turns
+ * into a status bit and the context stays usable.
+ */
+MSGL_API msgl_status msgl_selftest_wait_timeout(uint32_t *status, int64_t budget_cycles,
+                                                msgl_stream_t stream);
+
 /* Static description of a status code. */
 MSGL_API const char *msgl_status_string(msgl_status s);
 

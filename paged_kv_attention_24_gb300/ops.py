@@ -64,6 +64,7 @@ SIGNATURES = {
     "msgl_attn_decode": ([PP, PT, P, I32, P, I32, I32, F32, P, P, P, SZ, P, P], ctypes.c_int),
     "msgl_attn_decode_append": ([PP, PT, P, I32, P, P, P, P, I32, I32, F32, P, P, P, SZ, P, P], ctypes.c_int),
     "msgl_attn_decode_noalloc": ([PP, PT, P, I32, P, I32, I32, F32, P, P, P, P], ctypes.c_int),
+    "msgl_selftest_wait_timeout": ([P, I64, P], ctypes.c_int),
     "msgl_read_status": ([P, ctypes.POINTER(ctypes.c_uint32), P], ctypes.c_int),
     "msgl_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "msgl_last_error": ([], ctypes.c_char_p),
@@ -280,6 +281,12 @@ def attn_decode_noalloc(pool: KVPool, q: torch.Tensor, page_table: torch.Tensor,
         float(scale), _ptr(out), _ptr(lse), _ptr(status), _stream(stream))
     _check(rc, "msgl_attn_decode_noalloc")
     return out, lse
+
+
+def selftest_wait_timeout(status: torch.Tensor, budget_cycles: int = 10_000_000, stream=None) -> None:
+    """Run the bounded-wait self-test; the status word then holds DEVERR_TIMEOUT."""
+    rc = load().msgl_selftest_wait_timeout(_ptr(status), int(budget_cycles), _stream(stream))
+    _check(rc, "msgl_selftest_wait_timeout")
 
 
 def read_status(status: torch.Tensor, stream=None) -> int:

@@ -120,3 +120,22 @@ def test_status_word_accumulates_and_calls_continue():
     ref_o, _ = oracle.decode(d.q.cpu(), w.k_pool.cpu(), w.v_pool.cpu(), 1, d.page_table.cpu(),
                              d.seq_lens.cpu(), w.scale)
     assert_o_close(o, ref_o)
+
+
+def test_bounded_wait_times_out_into_status_and_context_survives():
+    """A wait that nothing satisfies gives up (about 5 ms here), sets the timeout bit, and later
+    calls still run and are exact."""
+    import time
+    status = ops.new_status()
+    t0 = time.time()
+    ops.selftest_wait_timeout(status, budget_cycles=10_000_000)
+    flags = ops.read_status(status)
+    assert flags == ops.DEVERR_TIMEOUT
+    assert time.time() - t0 < 5.0
+    w = W.make_workload("after_timeout", 16, 8, 128, 16, seed=9, decode_seq_lens=[200, 33], device="cuda")
+    d = w.decode
+    import oracle
+    o, lse = ops.attn_decode(ops.KVPool(w.k_pool, w.v_pool, 16), d.q, d.page_table, d.seq_lens, 200, w.scale)
+    ref_o, _ = oracle.decode(d.q.cpu(), w.k_pool.cpu(), w.v_pool.cpu(), 16, d.page_table.cpu(),
+                             d.seq_lens.cpu(), w.scale)
+    assert_o_close(o, ref_o)
