@@ -49,6 +49,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
+    ap.add_argument("--no-append", action="store_true", help="skip the fused append+decode timing")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="approximate CPU seconds for the oracle sample")
     return ap.parse_args(argv)
@@ -404,7 +405,7 @@ def run_ours(args):
         e2e = measure_e2e(args, w, pool, k_new, v_new, loc, dev, dec_bytes, ext_flops)
 
     append = None
-    if d is not None:
+    if d is not None and not args.no_append:
         # the decode batch through msgl_attn_decode_append (current-token K/V stored in the same launch)
         dk, dv = w.k_pool[d.new_loc.long()].contiguous(), w.v_pool[d.new_loc.long()].contiguous()
         for _ in range(3):
