@@ -7,8 +7,8 @@
 // Design (bandwidth-bound: every cached K/V byte is read exactly once)
 // ---------------------------------------------------------------------
 // * Balanced split-KV.  The keys of all requests, laid end to end, are cut
-//   into P equal ranges, one per persistent CTA (P = resident CTAs on the
-//   GPU).  A CTA's range covers one or more request segments; each segment
+//   into P equal ranges (at least 32 keys each), one per persistent CTA
+//   (P = resident CTAs on the GPU).  A CTA's range covers one or more request segments; each segment
 //   yields a partial (o, lse) per q head.  Request b's partials sit in rows
 //   b + i of the workspace, i over the CTAs whose ranges touch it, and the
 //   merge kernel folds them together by their log-sum-exp.
@@ -82,6 +82,14 @@ __device__ __forceinline__ long long warp_incl_scan(long long v, int lane) {
     return v;
 }
 
+// Keys per CTA range: an equal share, but at least two tiles, so that a small
+// batch does not scatter into hundreds of tiny partials for the merge to fold.
+constexpr long long kMinKeysPerCta = 2 * kTileKeys;
+__host__ __device__ __forceinline__ long long keys_per_cta(long long total, long long ctas) {
+    const long long share = (total + ctas - 1) / ctas;
+    return share > kMinKeysPerCta ? share : kMinKeysPerCta;
+}
+
 size_t stage_bytes(int hg) { return (size_t)2 * kTileKeys * (hg * 256 + 16); }
 
 size_t decode_smem_bytes(int hg, int stages) {
@@ -126,7 +134,7 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
         const long long P = gridDim.x;
-        const long long per = (total + P - 1) / P;
+        const long long per = keys_per_cta(total, P);
         const long long r0 = per * blockIdx.x;
         const long long r1 = min(total, r0 + per);
         int it = 0;
@@ -447,7 +455,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(
     }
     // the split kernel's partials are complete and visible after this point
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const long long per = (s_total + num_ctas - 1) / num_ctas;
+    const long long per = keys_per_cta(s_total, num_ctas);
     const int first = (int)(s_start / per);
     const int count = (int)((s_start + sb - 1) / per) - first + 1;   // <= num_ctas
     // max over the partial LSEs (NaN = failed segment)
