@@ -46,6 +46,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--page-size", type=int, default=None,
+                    help="override the workload's page size (same lengths and seeds)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
@@ -254,7 +256,7 @@ def run_reference(args):
     from paged_kv_attention_24_gb300 import workloads as W
     from paged_kv_attention_24_gb300 import accounting as A
     import oracle
-    w = W.config(args.config, device="cpu")
+    w = W.config(args.config, device="cpu", page_size=args.page_size)
     threads = oracle.default_threads()
     per_step = max(1.0, 90.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
@@ -275,7 +277,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * secs / max(1, args.steps), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": W.CONFIG_NAMES[args.config], "config_id": args.config,
+        "config": {"workload": w.name, "config_id": args.config,
                    "decode_kv_bytes_per_step": A.decode_kv_bytes(w),
                    "extend_flop_per_step": A.extend_flops(w)},
         "extend": {"value": statistics.mean(tf) if tf else None, "unit": "TFLOP/s"},
@@ -304,7 +306,7 @@ def run_ours(args):
     from paged_kv_attention_24_gb300 import workloads as W
     from paged_kv_attention_24_gb300 import accounting as A
 
-    w = W.config(args.config, device=dev, seed=1000 + args.config + 7 * rank)
+    w = W.config(args.config, device=dev, seed=1000 + args.config + 7 * rank, page_size=args.page_size)
     pool = ops.KVPool(w.k_pool, w.v_pool, w.page_size)
     k_new, v_new, loc = w.new_tokens()
     e, d = w.extend, w.decode
@@ -385,18 +387,18 @@ def run_ours(args):
     if d is not None:
         rooflines["decode"] = {"bound": "hbm", "achieved": per_gpu_dec, "peak": peaks["hbm_gbs"],
                                "unit": "GB/s", "frac": per_gpu_dec / peaks["hbm_gbs"],
-                               "traffic": recorded_traffic("decode", W.CONFIG_NAMES[args.config]),
+                               "traffic": recorded_traffic("decode", w.name),
                                "us_per_launch": dec_avg * 1e3}
     if e is not None:
         pk = peaks["bf16_tflops_sustained"]
         rooflines["extend"] = {"bound": "tensor", "achieved": per_gpu_ext, "peak": pk,
                                "unit": "TFLOP/s", "frac": per_gpu_ext / pk,
-                               "traffic": recorded_traffic("extend", W.CONFIG_NAMES[args.config]),
+                               "traffic": recorded_traffic("extend", w.name),
                                "us_per_launch": ext_avg * 1e3}
     if st_gbs:
         rooflines["store"] = {"bound": "hbm", "achieved": st_gbs, "peak": peaks["hbm_gbs"],
                               "unit": "GB/s", "frac": st_gbs / peaks["hbm_gbs"],
-                              "traffic": recorded_traffic("store", W.CONFIG_NAMES[args.config]),
+                              "traffic": recorded_traffic("store", w.name),
                               "us_per_launch": st_avg * 1e3}
     dominant = max(rooflines, key=lambda k: rooflines[k]["us_per_launch"])
 
@@ -442,7 +444,7 @@ def run_ours(args):
         "metric": METRIC, "value": dec_gbs, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": W.CONFIG_NAMES[args.config], "config_id": args.config,
+        "config": {"workload": w.name, "config_id": args.config,
                    "hq": w.hq, "hkv": w.hkv, "head_dim": w.d, "page_size": w.page_size,
                    "decode_batch": d.num_reqs if d else 0,
                    "extend_tokens": e.total_tokens if e else 0,

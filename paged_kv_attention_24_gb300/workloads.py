@@ -256,10 +256,12 @@ CONFIG_NAMES = {
 }
 
 
-def config(i: int, device="cpu", seed: Optional[int] = None, part: str = "all") -> Workload:
+def config(i: int, device="cpu", seed: Optional[int] = None, part: str = "all",
+           page_size: Optional[int] = None) -> Workload:
     """The five workloads (seed defaults to 1000 + i).
 
-    ``part`` = "decode" / "extend" keeps only that batch of a mixed config.
+    ``part`` = "decode" / "extend" keeps only that batch of a mixed config;
+    ``page_size`` overrides the config's page size (same lengths and seeds).
     """
     seed = 1000 + i if seed is None else seed
     rng = np.random.default_rng(seed + 7919)  # lengths; pool layout uses ``seed``
@@ -290,11 +292,20 @@ def config(i: int, device="cpu", seed: Optional[int] = None, part: str = "all") 
         shared = 2048
     else:
         raise ValueError(f"no config {i}")
+    if page_size is not None:
+        ps = int(page_size)
+        if shared and shared % ps:
+            raise ValueError("the shared prefix must be a whole number of pages")
+        if num_slots is not None and num_slots % ps:
+            num_slots = None
     if part == "decode":
         pre = ext = None
         shared = 0
     elif part == "extend":
         dec = None
-    return make_workload(CONFIG_NAMES[i] + ("" if part == "all" else f"-{part}"), hq, hkv, 128, ps,
+    name = CONFIG_NAMES[i] + ("" if part == "all" else f"-{part}")
+    if page_size is not None:
+        name += f"-page{ps}"
+    return make_workload(name, hq, hkv, 128, ps,
                          seed, decode_seq_lens=dec, extend_prefix_lens=pre, extend_ext_lens=ext,
                          shared_prefix_len=shared, num_slots=num_slots, device=device)
