@@ -13,18 +13,20 @@
 //   loaded by one 3D TMA box per 64-dim half straight from q[T, Hq, 128].
 //   Every K/V byte staged in shared memory feeds all G heads.
 // * A CTA owns two such tiles (2R tokens) of one request and one kv head and
-//   streams 128-key K and V tiles through 2-stage (K) and 3-stage (V) rings.  A page that is a
-//   contiguous, fully valid run of pool rows (page_size >= 16) arrives in one
-//   tiled TMA box per 64-dim half; any other keys are gathered four pool
-//   rows per copy (TMA gather4).  A key beyond the causal range, or behind a
-//   bad page id, gets a row index past the end of the pool, which TMA fills
-//   with zeros.
+//   streams 128-key K and V tiles through 2-stage (K) and 3-stage (V) rings.
+//   At page_size >= 16 a page that is a contiguous, fully valid run of pool
+//   rows arrives in one tiled TMA box per 64-dim half, and any other keys
+//   are gathered four pool rows per copy (TMA gather4).  Below 16 every key
+//   is its own run, and 16-byte cp.async copies replace the gathers (a TMA
+//   instruction per four 128-byte rows cannot keep up).  A key beyond the
+//   causal range, or behind a bad page id, reads as zeros.
 // * tcgen05.mma (M = N = 128, K = 16 per instruction, bf16 in, fp32 out):
 //   S_t = Q_t K^T lands in TMEM (columns 0-127 for tile 0, 128-255 for tile
 //   1); O_t accumulates in columns 256-383 / 384-511 (the whole 512-column
 //   TMEM of the SM).  P is written back over S_t as packed bf16 and fed to
 //   O_t += P_t V from TMEM, with V as an MN-major shared-memory operand.
-// * Warp roles: warp 0 issues TMA, one thread of warp 1 issues the MMAs,
+// * Warp roles: warp 0 loads Q and K, warp 3 loads V (warp 2 shares the K
+//   tiles on the cp.async path), one thread of warp 1 issues the MMAs,
 //   warps 4-7 and 8-11 run the online softmax of tile 0 and tile 1 (one
 //   TMEM lane = one row per thread).  While one warpgroup exponentiates,
 //   the tensor core works on the other tile.  O is rescaled lazily: only
@@ -165,9 +167,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ---------------------------------------------------------------- TMA producer
-        if (lane == 0) {
+    // Loaders: warp 0 brings Q and the K tiles, warp 3 the V tiles (one issuing warp per
+    // operand; a single warp issuing both was the bottleneck at small page sizes).  With
+    // no tiled boxes (page_size < 16) K/V rows are copied with 16-byte cp.async instead
+    // of TMA gathers, and warp 2 takes the odd K tiles so two K copies are in flight.
+    const bool lsu = a.box_rows == 0;
+    if (warp == 0 || warp == 3 || (lsu && warp == 2)) {
+        // ---------------------------------------------------------------- K/V loaders
+        const bool is_v = warp == 3;
+        if (warp == 0 && lane == 0) {
             const uint32_t box = 64u * G * a.q_box_rows * 2u;
             ptx::mbar_arrive_expect_tx(bar(kQFull), box * (nB > 0 ? 4u : 2u));
             for (int t = 0; t < (nB > 0 ? 2 : 1); ++t)
@@ -175,22 +183,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tma_load_3d(sbase + kOffQ + t * kTile + h * kHalf, &q_map, 64 * h, g * G,
                                      tok0 + t * R, bar(kQFull));
         }
-        int issued = 0;
-        // Keys come in 4-key groups, one per lane.  When a page is a contiguous run of
-        // pool rows (box_rows > 0), a fully valid box of box_rows keys is fetched by one
-        // tiled copy per 64-dim half, issued by the box's first lane; any other group is
-        // gathered four rows at a time, with out-of-range rows (zero fill) for keys past
-        // the causal range or behind a bad page id.
-        const int BR = a.box_rows;
-        const int lanes_per_box = BR > 0 ? BR / 4 : 1;
-        const int box_lead = (lane / lanes_per_box) * lanes_per_box;
-        const unsigned box_bits =
-            lanes_per_box >= 32 ? 0xffffffffu : ((1u << lanes_per_box) - 1u) << box_lead;
-        for (int j = 0; j < nkv && !*abort_flag; ++j) {
-            const int s = j & 1, rnd = j >> 1;
-            int rows[4];
-            bool all_ok = true;
-            int64_t slot0 = 0;
+        // Pool rows of the tile's keys, four consecutive keys per lane.  A key past the
+        // causal range or behind a bad page id gets oob_row (zero fill).
+        auto key_rows = [&](int j, int (&rows)[4], bool &all_ok, int64_t &slot0) {
+            all_ok = true;
+            slot0 = 0;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int key = j * kKeys + 4 * lane + e;
@@ -209,34 +206,89 @@ __global__ void __launch_bounds__(kThreads, 1)
                     all_ok = false;
                 }
             }
-            const unsigned ok_mask = __ballot_sync(0xffffffffu, all_ok);
-            const bool tiled = BR > 0 && (ok_mask & box_bits) == box_bits;
-            auto issue = [&](uint32_t dst, const CUtensorMap *gm, const CUtensorMap *tm, uint32_t fb) {
-                if (!tiled) {
-                    ptx::tma_gather4(dst, gm, 0, rows[0], rows[1], rows[2], rows[3], fb);
-                    ptx::tma_gather4(dst + kHalf, gm, 64, rows[0], rows[1], rows[2], rows[3], fb);
-                } else if (lane == box_lead) {
-                    ptx::tma_load_3d(dst, tm, 0, g, (int)slot0, fb);
-                    ptx::tma_load_3d(dst + kHalf, tm, 64, g, (int)slot0, fb);
+        };
+        int rows[4];
+        bool all_ok;
+        int64_t slot0;
+        if (lsu) {
+            // 16-byte cp.async copies into the SWIZZLE_128B K-major layout: per step, lanes
+            // 0-15 copy key 2i and lanes 16-31 key 2i + 1, one 16-byte chunk each (each key's
+            // 256-byte row is contiguous in the pool).  The rows of the next tile are looked
+            // up while the copies fly; writer-side proxy fence, then one arrival.
+            const __nv_bfloat16 *pool = is_v ? a.pool.v : a.pool.k;
+            const int step = is_v ? 1 : 2, first = warp == 2 ? 1 : 0;
+            const int hi = lane >> 4, c = lane & 15;
+            const uint32_t col_off = (uint32_t)(c >> 3) * kHalf;
+            int next[4];
+            if (first < nkv) key_rows(first, rows, all_ok, slot0);
+            for (int j = first; j < nkv && !*abort_flag; j += step) {
+                const int sv = j % kVStages;
+                const uint32_t empty = is_v ? bar(kVEmpty + sv) : bar(kKEmpty + (j & 1));
+                const uint32_t parity = is_v ? ((j / kVStages) & 1) ^ 1 : ((j >> 1) & 1) ^ 1;
+                if (!wait_or_abort(empty, parity, abort_flag, a.status)) break;
+                const uint32_t dst = is_v ? sbase + kOffV + sv * kTile : sbase + kOffK + (j & 1) * kTile;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    const int e0 = (i & 1) * 2;
+                    const int r0 = __shfl_sync(0xffffffffu, rows[e0], i >> 1);
+                    const int r1 = __shfl_sync(0xffffffffu, rows[e0 + 1], i >> 1);
+                    const int row = hi ? r1 : r0;
+                    const int r = 2 * i + hi;
+                    const bool valid = row < a.oob_row;
+                    ptx::cp_async_16(dst + col_off + (uint32_t)r * 128u + ((uint32_t)((c & 7) ^ (r & 7)) << 4),
+                                     pool + (valid ? (int64_t)row * kHeadDim + c * 8 : 0), valid ? 16u : 0u);
                 }
-            };
-            if (!wait_or_abort(bar(kKEmpty + s), (rnd & 1) ^ 1, abort_flag, a.status)) break;
-            if (lane == 0) ptx::mbar_arrive_expect_tx(bar(kKFull + s), kTile);
-            __syncwarp();
-            issue(sbase + kOffK + s * kTile + lane * 512, &k_map, &kt_map, bar(kKFull + s));
-            const int sv = j % kVStages, rv = j / kVStages;
-            if (!wait_or_abort(bar(kVEmpty + sv), (rv & 1) ^ 1, abort_flag, a.status)) { issued = j + 1; break; }
-            if (lane == 0) ptx::mbar_arrive_expect_tx(bar(kVFull + sv), kTile);
-            __syncwarp();
-            issue(sbase + kOffV + sv * kTile + lane * 512, &v_map, &vt_map, bar(kVFull + sv));
-            issued = j + 1;
-        }
-        if (*abort_flag) {
-            // let issued copies land before shared memory goes away (bounded waits)
-            ptx::mbar_wait(bar(kQFull), 0, 200000000LL);
-            for (int j = max(0, issued - kVStages); j < issued; ++j) {
-                if (j >= issued - kStages) ptx::mbar_wait(bar(kKFull + (j & 1)), (j >> 1) & 1, 200000000LL);
-                ptx::mbar_wait(bar(kVFull + (j % kVStages)), (j / kVStages) & 1, 200000000LL);
+                ptx::cp_async_commit();
+                if (j + step < nkv) key_rows(j + step, next, all_ok, slot0);
+                ptx::cp_async_wait_all();
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(is_v ? bar(kVFull + sv) : bar(kKFull + (j & 1)));
+#pragma unroll
+                for (int e = 0; e < 4; ++e) rows[e] = next[e];
+            }
+            ptx::cp_async_wait_all();
+            if (*abort_flag && warp == 0) ptx::mbar_wait(bar(kQFull), 0, 200000000LL);
+        } else {
+            // TMA: a page that is a contiguous run of pool rows and fully valid arrives in
+            // one tiled copy per 64-dim half, issued by its first lane; any other 4-key
+            // group is gathered four rows at a time.
+            const int BR = a.box_rows;
+            const int lanes_per_box = BR / 4;
+            const int box_lead = (lane / lanes_per_box) * lanes_per_box;
+            const unsigned box_bits =
+                lanes_per_box >= 32 ? 0xffffffffu : ((1u << lanes_per_box) - 1u) << box_lead;
+            const CUtensorMap *gm = is_v ? &v_map : &k_map;
+            const CUtensorMap *tm = is_v ? &vt_map : &kt_map;
+            int issued = 0;
+            for (int j = 0; j < nkv && !*abort_flag; ++j) {
+                key_rows(j, rows, all_ok, slot0);
+                const unsigned ok_mask = __ballot_sync(0xffffffffu, all_ok);
+                const bool tiled = (ok_mask & box_bits) == box_bits;
+                const int sv = j % kVStages;
+                const uint32_t empty = is_v ? bar(kVEmpty + sv) : bar(kKEmpty + (j & 1));
+                const uint32_t parity = is_v ? ((j / kVStages) & 1) ^ 1 : ((j >> 1) & 1) ^ 1;
+                if (!wait_or_abort(empty, parity, abort_flag, a.status)) break;
+                const uint32_t full = is_v ? bar(kVFull + sv) : bar(kKFull + (j & 1));
+                const uint32_t dst = (is_v ? sbase + kOffV + sv * kTile : sbase + kOffK + (j & 1) * kTile) + lane * 512;
+                if (lane == 0) ptx::mbar_arrive_expect_tx(full, kTile);
+                __syncwarp();
+                if (!tiled) {
+                    ptx::tma_gather4(dst, gm, 0, rows[0], rows[1], rows[2], rows[3], full);
+                    ptx::tma_gather4(dst + kHalf, gm, 64, rows[0], rows[1], rows[2], rows[3], full);
+                } else if (lane == box_lead) {
+                    ptx::tma_load_3d(dst, tm, 0, g, (int)slot0, full);
+                    ptx::tma_load_3d(dst + kHalf, tm, 64, g, (int)slot0, full);
+                }
+                issued = j + 1;
+            }
+            if (*abort_flag) {
+                // let issued copies land before shared memory goes away (bounded waits)
+                if (warp == 0) ptx::mbar_wait(bar(kQFull), 0, 200000000LL);
+                const int depth = is_v ? kVStages : kStages;
+                for (int j = max(0, issued - depth); j < issued; ++j)
+                    ptx::mbar_wait(is_v ? bar(kVFull + j % kVStages) : bar(kKFull + (j & 1)),
+                                   is_v ? (j / kVStages) & 1 : (j >> 1) & 1, 200000000LL);
             }
         }
     } else if (warp == 1) {

@@ -137,6 +137,17 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// 16-byte global -> shared copy through L2 (LDGSTS).  src_bytes = 0 writes 16
+// zero bytes and reads nothing (src must still be a valid address).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // ----------------------------------------------------------------- tcgen05
 // Shared-memory matrix descriptor, 128-byte swizzle (8-row x 128-byte atoms).
 // lbo / sbo in bytes: K-major tiles use (16, 1024); an MN-major operand uses
