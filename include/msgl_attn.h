@@ -254,6 +254,45 @@ MSGL_API msgl_status msgl_read_status(const uint32_t *status, uint32_t *flags, m
 MSGL_API msgl_status msgl_selftest_wait_timeout(uint32_t *status, int64_t budget_cycles,
                                                 msgl_stream_t stream);
 
+/*
+ * Host-side checks of one step's metadata, for tests and debugging.  They
+ * read HOST copies of the arrays (copy the device arrays back first), launch
+ * nothing, need no GPU and allocate nothing.  The kernels check the same
+ * conditions on the device and report them through the status word; these
+ * calls name the first offending entry in msgl_last_error().  Each returns
+ * MSGL_OK, MSGL_ERR_INVALID_ARG (NULL array, bad scalar, inconsistent
+ * lengths, wrong position, duplicate slot) or MSGL_ERR_OUT_OF_RANGE (a slot,
+ * page index or page id outside the pool or the table).
+ *
+ * msgl_check_store_meta:  every out_loc[t] lies in [0, num_slots) and no
+ *   slot is named twice (the store's result would depend on which row wins).
+ * msgl_check_extend_meta:  prefix_lens[b] >= 0, ext_lens[b] >= 0,
+ *   cu_ext[0] = 0, cu_ext[b+1] - cu_ext[b] = ext_lens[b], cu_ext[num_reqs] =
+ *   total_tokens, ext_lens[b] <= max_ext_len, prefix_lens[b] + ext_lens[b]
+ *   <= max_seq_len, positions[cu_ext[b] + i] = prefix_lens[b] + i (when
+ *   positions is non-NULL), and every page that keys 0..prefix_lens[b] +
+ *   ext_lens[b] - 1 fall on has an index below width and an id in
+ *   [0, num_slots / page_size).
+ * msgl_check_decode_meta:  1 <= seq_lens[b] <= max_seq_len and the pages of
+ *   keys 0..seq_lens[b] - 1 are in range as above.
+ *
+ * page_ids is host int32 [num_reqs, stride]; only the first width entries of
+ * a row are read.  The pages ("不懂SGLang？从miniSGLang开始", §1.3 item 3;
+ * "Mini-SGLang 实战指南", §6.1, §6.2) define what the metadata means; these
+ * checks have no counterpart there.
+ */
+MSGL_API msgl_status msgl_check_store_meta(int64_t num_slots, const int32_t *out_loc, int32_t n_tokens);
+
+MSGL_API msgl_status msgl_check_extend_meta(int64_t num_slots, int32_t page_size, const int32_t *page_ids,
+                                            int32_t stride, int32_t width, const int32_t *prefix_lens,
+                                            const int32_t *ext_lens, const int32_t *cu_ext,
+                                            const int32_t *positions, int32_t num_reqs, int32_t total_tokens,
+                                            int32_t max_ext_len, int32_t max_seq_len);
+
+MSGL_API msgl_status msgl_check_decode_meta(int64_t num_slots, int32_t page_size, const int32_t *page_ids,
+                                            int32_t stride, int32_t width, const int32_t *seq_lens,
+                                            int32_t num_reqs, int32_t max_seq_len);
+
 /* Static description of a status code. */
 MSGL_API const char *msgl_status_string(msgl_status s);
 

@@ -69,6 +69,9 @@ SIGNATURES = {
     "msgl_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "msgl_last_error": ([], ctypes.c_char_p),
     "msgl_abi_version": ([], I32),
+    "msgl_check_store_meta": ([I64, P, I32], ctypes.c_int),
+    "msgl_check_extend_meta": ([I64, I32, P, I32, I32, P, P, P, P, I32, I32, I32, I32], ctypes.c_int),
+    "msgl_check_decode_meta": ([I64, I32, P, I32, I32, P, I32, I32], ctypes.c_int),
 }
 
 
@@ -296,3 +299,52 @@ def read_status(status: torch.Tensor, stream=None) -> int:
     if rc not in (0, 4, 5):
         _check(rc, "msgl_read_status")
     return int(flags.value)
+
+
+# ------------------------------------------------------------ metadata checks (host)
+
+def _host_i32(t):
+    """A host int32 copy of a tensor (any device) or None, plus its ctypes pointer."""
+    if t is None:
+        return None, None
+    a = t.detach().to("cpu", torch.int32).contiguous()
+    return a, ctypes.c_void_p(a.data_ptr())
+
+
+def check_store_meta(out_loc: torch.Tensor, num_slots: int):
+    """Copies out_loc back and checks it: every slot in range, none twice.  Raises MsglError."""
+    a, p = _host_i32(out_loc)
+    _check(load().msgl_check_store_meta(int(num_slots), p, a.numel()), "msgl_check_store_meta")
+
+
+def _table(page_table: torch.Tensor):
+    a, p = _host_i32(page_table)
+    if a.dim() == 1:
+        a = a.reshape(1, -1)
+    return a, p, int(a.shape[1])
+
+
+def check_extend_meta(num_slots: int, page_size: int, page_table: torch.Tensor, prefix_lens: torch.Tensor,
+                      ext_lens: torch.Tensor, cu_ext: torch.Tensor, positions: Optional[torch.Tensor],
+                      max_ext_len: int, max_seq_len: int):
+    """Copies an extend step's metadata back and checks it (lengths, positions, pages).  Raises MsglError."""
+    pt, ptp, w = _table(page_table)
+    pre, prep = _host_i32(prefix_lens)
+    ext, extp = _host_i32(ext_lens)
+    cu, cup = _host_i32(cu_ext)
+    pos, posp = _host_i32(positions)
+    if cu.numel() != pre.numel() + 1 or ext.numel() != pre.numel():
+        raise ValueError("cu_ext must have num_reqs + 1 entries and ext_lens num_reqs")
+    total = int(pos.numel()) if pos is not None else int(cu[-1])
+    _check(load().msgl_check_extend_meta(int(num_slots), int(page_size), ptp, w, w, prep, extp, cup, posp,
+                                         pre.numel(), total, int(max_ext_len), int(max_seq_len)),
+           "msgl_check_extend_meta")
+
+
+def check_decode_meta(num_slots: int, page_size: int, page_table: torch.Tensor, seq_lens: torch.Tensor,
+                      max_seq_len: int):
+    """Copies a decode step's metadata back and checks it (lengths, pages).  Raises MsglError."""
+    pt, ptp, w = _table(page_table)
+    seq, seqp = _host_i32(seq_lens)
+    _check(load().msgl_check_decode_meta(int(num_slots), int(page_size), ptp, w, w, seqp, seq.numel(),
+                                         int(max_seq_len)), "msgl_check_decode_meta")
