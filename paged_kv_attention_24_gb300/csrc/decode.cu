@@ -458,6 +458,45 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(
     const long long per = keys_per_cta(s_total, num_ctas);
     const int first = (int)(s_start / per);
     const int count = (int)((s_start + sb - 1) / per) - first + 1;   // <= num_ctas
+    if (count <= 4) {
+        // few partials (the usual case): every lane loads all partial LSEs and its four dims
+        // of every partial row at once, so the fold costs one memory round trip
+        const float *lp = part_lse + (long long)(b + first) * hq + h;
+        const float *op = part_o + ((long long)(b + first) * hq + h) * kHeadDim + lane * 4;
+        const long long stride = (long long)hq * kHeadDim;
+        float x[4];
+        float4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[i] = i < count ? lp[(long long)i * hq] : -INFINITY;
+            v[i] = i < count ? *reinterpret_cast<const float4 *>(op + i * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        bool bad = false;
+        float M = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            bad |= isnan(x[i]);
+            M = fmaxf(M, x[i]);
+        }
+        float L = 0.f, acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+        if (!bad && M != -INFINITY) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float w = x[i] == -INFINITY ? 0.f : __expf(x[i] - M);
+                L += w;
+                acc0 += w * v[i].x;
+                acc1 += w * v[i].y;
+                acc2 += w * v[i].z;
+                acc3 += w * v[i].w;
+            }
+        }
+        const bool zero = bad || !(L > 0.f);
+        const float inv = zero ? 0.f : 1.f / L;
+        *reinterpret_cast<uint2 *>(orow) =
+            make_uint2(ptx::pack_bf16(acc0 * inv, acc1 * inv), ptx::pack_bf16(acc2 * inv, acc3 * inv));
+        if (lane == 0) lse[row] = zero ? -INFINITY : M + logf(L);
+        return;
+    }
     // max over the partial LSEs (NaN = failed segment)
     float M = -INFINITY;
     bool failed = false;

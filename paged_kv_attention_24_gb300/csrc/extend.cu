@@ -468,12 +468,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         w.y = ptx::pack_bf16(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
                         w.z = ptx::pack_bf16(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
                         w.w = ptx::pack_bf16(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
-                        dst[q] = w;
+                        __stcs(reinterpret_cast<int4 *>(dst) + q, make_int4((int)w.x, (int)w.y, (int)w.z, (int)w.w));
                     }
                 }
             }
             if (store) {
-                a.lse[orow] = (m_ref + log2f(l)) * kLn2;
+                __stcs(a.lse + orow, (m_ref + log2f(l)) * kLn2);
                 if (a.positions && jh == 0 && __ldg(a.positions + tok_g) != limit)
                     report(a.status, MSGL_DEVERR_POSITION);
             }
