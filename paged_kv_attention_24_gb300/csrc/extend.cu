@@ -394,13 +394,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 128; ++i)
                     if (i > lim) v[i] = __float_as_uint(-INFINITY);
             }
-            float mxa = -INFINITY, mxb = -INFINITY;
+            // row max in four independent 3-input chains (16 deep each)
+            float mxa = -INFINITY, mxb = -INFINITY, mxc = -INFINITY, mxd = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < 128; i += 4) {
+            for (int i = 0; i < 128; i += 8) {
                 mxa = ptx::max3(mxa, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
                 mxb = ptx::max3(mxb, __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                mxc = ptx::max3(mxc, __uint_as_float(v[i + 4]), __uint_as_float(v[i + 5]));
+                mxd = ptx::max3(mxd, __uint_as_float(v[i + 6]), __uint_as_float(v[i + 7]));
             }
-            const float m_new = fmaxf(m_ref, fmaxf(mxa, mxb) * a.scale_log2);
+            const float m_new = fmaxf(m_ref, fmaxf(fmaxf(mxa, mxb), fmaxf(mxc, mxd)) * a.scale_log2);
             const bool need = m_new > m_ref + 8.f;
             if (j > 0 && __any_sync(0xffffffffu, need)) {
                 const float alpha = need ? ptx::ex2(m_ref - m_new) : 1.f;
