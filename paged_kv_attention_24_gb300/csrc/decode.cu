@@ -140,6 +140,8 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
         int it = 0;
         bool aborted = false;
         const uint32_t row_bytes = (uint32_t)hg * 256;
+        // every K/V byte is read once: evict-first keeps the stream from displacing other lines
+        const uint64_t stream_policy = ptx::l2_evict_first_policy();
         const long long slot_elems = (long long)a.pool.hkv * kHeadDim;
 
         auto stage_wait_empty = [&](int stage, int round) -> bool {
@@ -216,10 +218,10 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
                             uint8_t *vdst = kdst + kTileKeys * pitch;
                             const long long off = slot * slot_elems + (long long)g0 * kHeadDim;
                             const long long noff = (long long)b * slot_elems + (long long)g0 * kHeadDim;
-                            ptx::bulk_g2s(ptx::smem_u32(kdst), is_new ? a.k_new + noff : a.pool.k + off,
-                                          row_bytes, full_bar);
-                            ptx::bulk_g2s(ptx::smem_u32(vdst), is_new ? a.v_new + noff : a.pool.v + off,
-                                          row_bytes, full_bar);
+                            ptx::bulk_g2s_hint(ptx::smem_u32(kdst), is_new ? a.k_new + noff : a.pool.k + off,
+                                               row_bytes, full_bar, stream_policy);
+                            ptx::bulk_g2s_hint(ptx::smem_u32(vdst), is_new ? a.v_new + noff : a.pool.v + off,
+                                               row_bytes, full_bar, stream_policy);
                         }
                         if (has_new) {
                             // write the new K/V rows of this head group into the pool at new_loc[b];
