@@ -323,14 +323,34 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
             seg_bad |= (flags & kBad) != 0;
 
             const uint32_t base = tiles + (uint32_t)(stage * sbytes);
-            // S^T (16 keys x 8 q-head slots) = K (16 x 128) * Q^T (128 x 8)
-            float s[4] = {0.f, 0.f, 0.f, 0.f};
+            // Read the whole stage (K and V fragments) into registers, then hand it back:
+            // the producer's next copies into this stage overlap the math below.  The
+            // arrival's address depends on the loaded registers, so it cannot pass them.
+            uint32_t kf[8][4], vf[8][4];
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                uint32_t af[4];
-                ptx::ldsm_x4(base + k_lane + ks * 32, af[0], af[1], af[2], af[3]);
-                ptx::mma_bf16_16816(s, af, qf[ks][0], qf[ks][1]);
+            for (int ks = 0; ks < 8; ++ks)
+                ptx::ldsm_x4(base + k_lane + ks * 32, kf[ks][0], kf[ks][1], kf[ks][2], kf[ks][3]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                ptx::ldsm_x4_t(base + v_lane + i * 32, vf[i][0], vf[i][1], vf[i][2], vf[i][3]);
+            {
+                uint32_t any = 0u;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) any |= kf[i][0] | vf[i][0];
+                uint32_t zero;
+                asm volatile("and.b32 %0, %1, 0;" : "=r"(zero) : "r"(any));
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(empty + stage) + zero);
             }
+            // S^T (16 keys x 8 q-head slots) = K (16 x 128) * Q^T (128 x 8), two accumulation chains
+            float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 8; ks += 2) {
+                ptx::mma_bf16_16816(s, kf[ks], qf[ks][0], qf[ks][1]);
+                ptx::mma_bf16_16816(s2, kf[ks + 1], qf[ks + 1][0], qf[ks + 1][1]);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) s[i] += s2[i];
             const bool v0 = (mask >> k0) & 1u, v1 = (mask >> k1) & 1u;
             const float x00 = v0 ? s[0] * a.scale_log2 : -INFINITY;   // key k0, head h0
             const float x01 = v0 ? s[1] * a.scale_log2 : -INFINITY;   // key k0, head h1
@@ -343,12 +363,12 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
             }
             const float mn0 = fmaxf(m2[0], mx0), mn1 = fmaxf(m2[1], mx1);
-            const float al0 = (mn0 == -INFINITY) ? 1.f : exp2f(m2[0] - mn0);
-            const float al1 = (mn1 == -INFINITY) ? 1.f : exp2f(m2[1] - mn1);
-            const float p00 = (x00 == -INFINITY) ? 0.f : exp2f(x00 - mn0);
-            const float p01 = (x01 == -INFINITY) ? 0.f : exp2f(x01 - mn1);
-            const float p10 = (x10 == -INFINITY) ? 0.f : exp2f(x10 - mn0);
-            const float p11 = (x11 == -INFINITY) ? 0.f : exp2f(x11 - mn1);
+            const float al0 = (mn0 == -INFINITY) ? 1.f : ptx::ex2(m2[0] - mn0);
+            const float al1 = (mn1 == -INFINITY) ? 1.f : ptx::ex2(m2[1] - mn1);
+            const float p00 = (x00 == -INFINITY) ? 0.f : ptx::ex2(x00 - mn0);
+            const float p01 = (x01 == -INFINITY) ? 0.f : ptx::ex2(x01 - mn1);
+            const float p10 = (x10 == -INFINITY) ? 0.f : ptx::ex2(x10 - mn0);
+            const float p11 = (x11 == -INFINITY) ? 0.f : ptx::ex2(x11 - mn1);
             m2[0] = mn0;
             m2[1] = mn1;
             l[0] = l[0] * al0 + p00 + p10;
@@ -360,20 +380,16 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
             const uint32_t mb = ((mask >> kv1) & 1u ? 0x0000ffffu : 0u) | ((mask >> (kv1 + 1)) & 1u ? 0xffff0000u : 0u);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                uint32_t af[4];
-                ptx::ldsm_x4_t(base + v_lane + i * 32, af[0], af[1], af[2], af[3]);
-                af[0] &= ma;
-                af[1] &= ma;
-                af[2] &= mb;
-                af[3] &= mb;
+                vf[i][0] &= ma;
+                vf[i][1] &= ma;
+                vf[i][2] &= mb;
+                vf[i][3] &= mb;
                 acc[i][0] *= al0;
                 acc[i][1] *= al1;
                 acc[i][2] *= al0;
                 acc[i][3] *= al1;
-                ptx::mma_bf16_16816(acc[i], af, pb0, pb1);
+                ptx::mma_bf16_16816(acc[i], vf[i], pb0, pb1);
             }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(empty + stage));
 
             if (flags & kLast) {
                 float lt0 = l[0], lt1 = l[1];
