@@ -12,21 +12,28 @@
 //   yields a partial (o, lse) per q head.  Request b's partials sit in rows
 //   b + i of the workspace, i over the CTAs whose ranges touch it, and the
 //   merge kernel folds them together by their log-sum-exp.
-// * One CTA handles a group of up to 8 kv heads (all of them for Hkv <= 8),
-//   so each key's pool row (Hkv * 256 bytes, contiguous in the slot-major
-//   pool) arrives in one bulk copy.  A producer warp resolves slots through
-//   the page table (range-checked) and issues one cp.async.bulk per key for
-//   K and one for V into a ring of 16-key stages; rows land at a pitch of
-//   row + 16 bytes so that ldmatrix over 8 consecutive keys is free of bank
-//   conflicts.  Stages are handed over with mbarriers (full: bytes landed;
-//   empty: every consumer warp is done with the stage).
+// * One CTA handles a group of up to 8 kv heads (all of them for Hkv <= 8).
+//   A producer warp resolves slots through the page table (range-checked)
+//   and fills a ring of 16-key stages; stages are handed over with mbarriers
+//   (full: bytes landed; empty: every consumer warp has read the stage).
+//   - page_size >= 16 ("box" path): a 16-key tile aligned to 16 keys lies in
+//     one page, so its K (and V) arrive as two 3D TMA boxes of 64 dims x 16
+//     keys x the group's heads (128-byte swizzle, head-major rows).  Four
+//     copies per stage: a TMA unit issues about one copy per 80 cycles, which
+//     held per-key copies near 50 GB/s per SM.
+//   - page_size < 16, or the append mode: each key's pool row (the group's
+//     heads, contiguous in the slot-major pool) arrives in one cp.async.bulk
+//     for K and one for V, at a pitch of row + 16 bytes so that ldmatrix over
+//     8 consecutive keys is free of bank conflicts.
 // * One consumer warp per kv head computes S^T = K Q^T with m16n8k16 MMAs
 //   (M = 16 keys, N = the group's 8 q-head slots, K = 128 dims), keeps a
 //   base-2 online softmax per q head, transposes P to the B operand with
 //   movmatrix, and accumulates O^T = V^T P^T (M = 16 dims x 8 tiles).
 //   Packing the q heads of a kv head into N means each KV byte feeds all G
 //   q heads at once.
+#include <limits.h>
 #include <math.h>
+#include <string.h>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -90,18 +97,28 @@ __host__ __device__ __forceinline__ long long keys_per_cta(long long total, long
     return share > kMinKeysPerCta ? share : kMinKeysPerCta;
 }
 
-size_t stage_bytes(int hg) { return (size_t)2 * kTileKeys * (hg * 256 + 16); }
-
-size_t decode_smem_bytes(int hg, int stages) {
-    return stages * stage_bytes(hg) + stages * sizeof(TileMeta) + 2 * stages * sizeof(uint64_t) + 16;
+// Bytes of one stage: K and V of 16 keys for hg heads.  Box stages hold four swizzled
+// 64-dim halves (K0, K1, V0, V1) of hg x 16 rows of 128 bytes; per-key stages hold
+// padded rows.
+size_t stage_bytes(int hg, bool box) {
+    return box ? (size_t)4 * hg * kTileKeys * 128 : (size_t)2 * kTileKeys * (hg * 256 + 16);
 }
 
+// + 1024: the box path aligns the stage ring to 1024 bytes (128-byte swizzle atoms)
+size_t decode_smem_bytes(int hg, int stages, bool box) {
+    return 1024 + stages * stage_bytes(hg, box) + stages * sizeof(TileMeta) + 2 * stages * sizeof(uint64_t) + 16;
+}
+
+template <bool kBox>
 __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
-    decode_split_kernel(const DecodeKernelArgs a) {
-    extern __shared__ __align__(128) uint8_t smem[];
+    decode_split_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
+                        const DecodeKernelArgs a) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
     const int hg = a.hg;
     const int pitch = hg * 256 + 16;
-    const int sbytes = 2 * kTileKeys * pitch;
+    const int half_bytes = hg * kTileKeys * 128;   // box path: one 64-dim half of K or V
+    const int sbytes = kBox ? 4 * half_bytes : 2 * kTileKeys * pitch;
     const int S = a.stages;
     TileMeta *meta = reinterpret_cast<TileMeta *>(smem + (size_t)S * sbytes);
     uint64_t *full = reinterpret_cast<uint64_t *>(meta + S);
@@ -179,6 +196,48 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
                         const int pidx = key >> a.pool.log2_ps;
                         return pidx < a.pages.width ? __ldg(a.pages.ids + (int64_t)b * a.pages.stride + pidx) : -1;
                     };
+                    if constexpr (kBox) {
+                        // 16-key tiles aligned to 16 keys (each inside one page); keys outside
+                        // [lo, hi) are loaded with the tile and masked.  Lane 0 does the work,
+                        // with the next tile's page id looked up one tile ahead.
+                        const int tlo = lo & ~(kTileKeys - 1);
+                        int pid_cur = lane == 0 ? load_pid(tlo) : -1;
+                        for (int t0 = tlo; t0 < hi; t0 += kTileKeys) {
+                            const int stage = it % S, round = it / S;
+                            const int t1 = t0 + kTileKeys;
+                            const int pid_next = (lane == 0 && t1 < hi) ? load_pid(t1) : -1;
+                            if (*abort_flag || !stage_wait_empty(stage, round)) { aborted = true; break; }
+                            if (lane == 0) {
+                                const int klo = max(lo, t0) - t0, khi = min(hi, t1) - t0;
+                                const uint32_t keys = ((1u << khi) - 1u) & ~((1u << klo) - 1u);
+                                const bool ok = pid_cur >= 0 && pid_cur < a.pool.num_pages;
+                                const uint32_t full_bar = ptx::smem_u32(full + stage);
+                                TileMeta &md = meta[stage];
+                                md.b = b;
+                                md.slot = b + (int)blockIdx.x;
+                                md.n = khi - klo;
+                                md.flags = (t0 == tlo ? kFirst : 0) | (t1 >= hi ? kLast : 0) | (ok ? 0 : kBad);
+                                md.mask = ok ? keys : 0u;
+                                if (!ok) report(a.status, MSGL_DEVERR_PAGE_RANGE);
+                                ptx::mbar_arrive_expect_tx(full_bar, ok ? (uint32_t)sbytes : 0u);
+                                if (ok) {
+                                    const int slot0 = (pid_cur << a.pool.log2_ps) + (t0 & ((1 << a.pool.log2_ps) - 1));
+                                    const uint32_t dst = ptx::smem_u32(smem + (size_t)stage * sbytes);
+                                    ptx::tma_load_3d_hint(dst, &k_map, 0, slot0, g0, full_bar, stream_policy);
+                                    ptx::tma_load_3d_hint(dst + half_bytes, &k_map, 64, slot0, g0, full_bar, stream_policy);
+                                    ptx::tma_load_3d_hint(dst + 2 * half_bytes, &v_map, 0, slot0, g0, full_bar, stream_policy);
+                                    ptx::tma_load_3d_hint(dst + 3 * half_bytes, &v_map, 64, slot0, g0, full_bar, stream_policy);
+                                }
+                            }
+                            pid_cur = pid_next;
+                            __syncwarp();
+                            ++it;
+                        }
+                        pos = min(r1, end_b);
+                        start_b = end_b;
+                        ++b;
+                        continue;
+                    }
                     // the page ids of the next tile are loaded one tile ahead, so the table
                     // lookup overlaps the wait for a free stage
                     int pid_cur = lane < min(kTileKeys, hi - lo) ? load_pid(lo + lane) : -1;
@@ -289,6 +348,13 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
         const int vcol = 8 * ((lane >> 3) & 1);
         const uint32_t k_lane = (uint32_t)(krow * pitch + warp * 256 + kcol * 2);
         const uint32_t v_lane = (uint32_t)(kTileKeys * pitch + vrow * pitch + warp * 256 + vcol * 2);
+        // Box path: row (head w, key k) of a 64-dim half sits at (16 w + k) * 128 bytes, its
+        // 16-byte chunk c at position c ^ (k & 7) (k & 7 = lane & 7 for every ldmatrix row
+        // this lane addresses).  Offset of dims [d, d + 8) of this lane's K / V row:
+        auto box_off = [&](int row, int d) -> uint32_t {
+            return (uint32_t)((d >> 6) * half_bytes + (warp * kTileKeys + row) * 128 +
+                              ((((d & 63) >> 3) ^ (lane & 7)) << 4));
+        };
 
         for (int it = 0;; ++it) {
             const int stage = it % S, round = it / S;
@@ -328,11 +394,16 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
             // arrival's address depends on the loaded registers, so it cannot pass them.
             uint32_t kf[8][4], vf[8][4];
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                ptx::ldsm_x4(base + k_lane + ks * 32, kf[ks][0], kf[ks][1], kf[ks][2], kf[ks][3]);
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t addr = kBox ? base + box_off(krow, 16 * ks + kcol) : base + k_lane + ks * 32;
+                ptx::ldsm_x4(addr, kf[ks][0], kf[ks][1], kf[ks][2], kf[ks][3]);
+            }
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                ptx::ldsm_x4_t(base + v_lane + i * 32, vf[i][0], vf[i][1], vf[i][2], vf[i][3]);
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t addr =
+                    kBox ? base + 2 * half_bytes + box_off(vrow, 16 * i + vcol) : base + v_lane + i * 32;
+                ptx::ldsm_x4_t(addr, vf[i][0], vf[i][1], vf[i][2], vf[i][3]);
+            }
             {
                 uint32_t any = 0u;
 #pragma unroll
@@ -578,12 +649,12 @@ struct Launch {
     size_t smem;
 };
 
-Launch decode_launch_shape(int hkv) {
+Launch decode_launch_shape(int hkv, bool box) {
     Launch L;
     L.hg = hkv <= kMaxHeadGroup ? hkv : kMaxHeadGroup;
-    int st = (int)((kSmemBudget - 64) / (stage_bytes(L.hg) + sizeof(TileMeta) + 16));
+    int st = (int)((kSmemBudget - 1024 - 64) / (stage_bytes(L.hg, box) + sizeof(TileMeta) + 16));
     L.stages = st < 2 ? 2 : (st > kMaxStages ? kMaxStages : st);
-    L.smem = decode_smem_bytes(L.hg, L.stages);
+    L.smem = decode_smem_bytes(L.hg, L.stages, box);
     static int sm_count[64];   // per device, filled on first use (same value if two threads race)
     int dev = 0;
     cudaGetDevice(&dev);
@@ -617,14 +688,39 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     if (a.num_reqs == 0) return cudaSuccess;
     const int hkv = a.pool.hkv;
     if (hkv > kMaxHeadGroup && hkv % kMaxHeadGroup != 0) return cudaErrorInvalidValue;
-    const Launch L = decode_launch_shape(hkv);
+    // Box path: whole 16-key tiles by 3D TMA (page_size >= 16, not the append mode).  Its
+    // tensor maps view each pool as [kv head][slot][128 dims] (innermost last), so a box
+    // lands head-major: 16 consecutive keys of one head form 16 consecutive smem rows.
+    const int hg = hkv <= kMaxHeadGroup ? hkv : kMaxHeadGroup;
+    bool box = a.new_loc == nullptr && (1 << a.pool.log2_ps) >= kTileKeys && a.pool.num_slots < INT_MAX;
+    CUtensorMap km, vm;
+    memset(&km, 0, sizeof km);
+    memset(&vm, 0, sizeof vm);
+    if (box) {
+        PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+        if (!enc) return cudaErrorNotSupported;
+        for (int which = 0; which < 2; ++which) {
+            cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)a.pool.num_slots, (cuuint64_t)hkv};
+            cuuint64_t strides[2] = {(cuuint64_t)hkv * kHeadDim * 2, (cuuint64_t)kHeadDim * 2};
+            cuuint32_t boxd[3] = {64, (cuuint32_t)kTileKeys, (cuuint32_t)hg};
+            cuuint32_t es[3] = {1, 1, 1};
+            if (enc(which ? &vm : &km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                    const_cast<__nv_bfloat16 *>(which ? a.pool.v : a.pool.k), dims, strides, boxd, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return cudaErrorInvalidValue;
+        }
+    }
+    const Launch L = decode_launch_shape(hkv, box);
     static bool attr_set[64];   // per device; idempotent, racing setters write the same value
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(decode_split_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBudget);
+        cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(decode_split_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmemBudget);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
@@ -649,7 +745,10 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     (void)plan;
     if (L.smem > (size_t)kSmemBudget) return cudaErrorInvalidValue;
     dim3 grid(L.ctas, hkv / L.hg);
-    decode_split_kernel<<<grid, 32 * (L.hg + 1), L.smem, stream>>>(k);
+    if (box)
+        decode_split_kernel<true><<<grid, 32 * (L.hg + 1), L.smem, stream>>>(km, vm, k);
+    else
+        decode_split_kernel<false><<<grid, 32 * (L.hg + 1), L.smem, stream>>>(km, vm, k);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // programmatic dependent launch: the merge's launch and its seq_lens scan overlap the

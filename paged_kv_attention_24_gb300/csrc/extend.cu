@@ -511,7 +511,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+}  // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
         void *p = nullptr;
@@ -524,8 +526,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-}  // namespace
-
 size_t extend_workspace_bytes(int32_t, int32_t, int32_t, int32_t, int32_t) { return 0; }
 
 cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t stream) {
@@ -534,7 +534,7 @@ cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t stream) {
     const int G = a.hq / hkv;
     const int R = kRows / G;
     const int q_box_rows = R < a.total_tokens ? R : a.total_tokens;
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
 
     CUtensorMap qm, km, vm;

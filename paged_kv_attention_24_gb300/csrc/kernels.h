@@ -1,6 +1,8 @@
 // Launchers shared between the C-ABI layer (api.cu) and the kernel files.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -56,6 +58,9 @@ struct ExtendArgs {
     uint32_t *status;
 };
 cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t stream);
+
+// cuTensorMapEncodeTiled from the driver (NULL if unavailable); looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // Sets the text msgl_last_error() returns on this thread.
 void set_last_error(const char *msg);

@@ -141,6 +141,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int 
         : "memory");
 }
 
+// tma_load_3d with an L2 cache policy
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tmap, int c0, int c1, int c2,
+                                                 uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+        "[%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // Four rows (one 64-element box each) of a 2D tensor map, gathered by row index.
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int col, int r0, int r1,
                                             int r2, int r3, uint32_t bar) {

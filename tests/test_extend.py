@@ -189,15 +189,17 @@ def test_extend_long_prefix_many_tiles():
     assert_lse_close(lse, ref_l)
 
 
-def test_extend_bad_page_zeroes_affected_rows():
-    """A page id past the pool: status bit set; rows that would read it are zero, earlier rows exact."""
-    ps = 16
+@pytest.mark.parametrize("ps", [1, 4, 16])
+def test_extend_bad_page_zeroes_affected_rows(ps):
+    """A page id past the pool: status bit set; rows that would read it are zero, earlier rows exact.
+
+    Page sizes below 16 take the cp.async copy path, 16 the TMA path."""
     w = W.make_workload("badpage", 16, 8, 128, ps, seed=51, extend_prefix_lens=[64], extend_ext_lens=[100],
                         device="cuda")
     e = w.extend
     good_o, good_l = run_gpu(w)
     pt = e.page_table.clone()
-    bad_page_idx = 7                                   # keys 112..127 -> chunk rows i >= 48
+    bad_page_idx = 112 // ps                           # first bad key 112 -> chunk rows i >= 48
     pt[0, bad_page_idx] = w.num_slots // ps + 3
     pool = ops.KVPool(w.k_pool, w.v_pool, ps)
     status = ops.new_status()
@@ -210,9 +212,10 @@ def test_extend_bad_page_zeroes_affected_rows():
     assert torch.equal(o[:first_bad_row], good_o[:first_bad_row])
 
 
-def test_extend_zero_length_requests_and_graph_replay():
+@pytest.mark.parametrize("ps", [1, 16])
+def test_extend_zero_length_requests_and_graph_replay(ps):
     """Requests with no chunk tokens write nothing; a captured extend replays with new inputs."""
-    w = W.make_workload("zero", 40, 8, 128, 16, seed=52, extend_prefix_lens=[10, 500, 0],
+    w = W.make_workload("zero", 40, 8, 128, ps, seed=52, extend_prefix_lens=[10, 500, 0],
                         extend_ext_lens=[0, 70, 33], device="cuda")
     e = w.extend
     pool = ops.KVPool(w.k_pool, w.v_pool, w.page_size)
