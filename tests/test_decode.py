@@ -44,7 +44,7 @@ def test_decode_configs(cfg):
 
 
 @pytest.mark.parametrize("ps", [1, 2, 8, 16, 32, 64, 128, 256])
-@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (32, 8), (40, 8), (64, 8), (4, 1), (10, 2)])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (32, 8), (40, 8), (64, 8), (4, 1), (10, 2), (32, 16), (48, 24)])
 def test_decode_shapes(ps, hq, hkv):
     seqs = [1, 2, ps - 1 if ps > 1 else 3, ps, ps + 1, 2 * ps + 3, 77, 1000, 4099]
     w = W.make_workload("shapes", hq, hkv, 128, ps, seed=ps * 100 + hq, decode_seq_lens=seqs, device="cuda")

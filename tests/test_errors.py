@@ -29,6 +29,25 @@ def test_bad_page_id_sets_status_and_zeroes_only_that_row():
     assert torch.equal(o[0], good_o[0]) and torch.equal(o[2], good_o[2])
 
 
+@pytest.mark.parametrize("ps", [1, 64])
+def test_bad_page_inside_a_long_request(ps):
+    """A bad page id deep inside a long request (page size 64 takes the TMA box copies, 1 the
+    per-key copies): only that request's row is zeroed; the others match the clean run."""
+    seqs = [3000, 2500, 700, 4100]
+    w = W.make_workload("badmid", 32, 8, 128, ps, seed=11, decode_seq_lens=seqs, device="cuda")
+    d = w.decode
+    pool = ops.KVPool(w.k_pool, w.v_pool, ps)
+    good_o, good_l = ops.attn_decode(pool, d.q, d.page_table, d.seq_lens, d.max_seq_len, w.scale)
+    pt = d.page_table.clone()
+    pt[1, 1337 // ps] = -3
+    status = ops.new_status()
+    o, lse = ops.attn_decode(pool, d.q, pt, d.seq_lens, d.max_seq_len, w.scale, status=status)
+    assert ops.read_status(status) & ops.DEVERR_PAGE_RANGE
+    assert torch.all(o[1] == 0) and torch.all(lse[1] == float("-inf"))
+    for b in (0, 2, 3):
+        assert torch.equal(o[b], good_o[b]) and torch.equal(lse[b], good_l[b])
+
+
 def test_short_page_table_is_a_range_error():
     w = W.make_workload("short", 16, 8, 128, 16, seed=2, decode_seq_lens=[100], device="cuda")
     d = w.decode
