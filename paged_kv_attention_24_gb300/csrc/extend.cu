@@ -457,21 +457,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool store = row_valid && tok_g < a.total_tokens;
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const long long orow = ((long long)tok_g * a.hq + (long long)g * G + jh);
+            const bool o_aligned32 = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t v[32];
                 ptx::tc_ld32(tO + 32 * c, v);
                 ptx::tc_wait_ld();
                 if (store) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(a.o + orow * kHeadDim + 32 * c);
+                    __nv_bfloat16 *dst = a.o + orow * kHeadDim + 32 * c;
+                    uint32_t w[16];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint4 w;
-                        w.x = ptx::pack_bf16(__uint_as_float(v[8 * q + 0]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
-                        w.y = ptx::pack_bf16(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
-                        w.z = ptx::pack_bf16(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
-                        w.w = ptx::pack_bf16(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
-                        __stcs(reinterpret_cast<int4 *>(dst) + q, make_int4((int)w.x, (int)w.y, (int)w.z, (int)w.w));
+                    for (int q = 0; q < 16; ++q)
+                        w[q] = ptx::pack_bf16(__uint_as_float(v[2 * q]) * inv, __uint_as_float(v[2 * q + 1]) * inv);
+                    if (o_aligned32) {
+                        // 32-byte streaming stores: half the store instructions of 16-byte ones
+                        ptx::st_cs_v8(dst, w);
+                        ptx::st_cs_v8(dst + 16, w + 8);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            __stcs(reinterpret_cast<int4 *>(dst) + q,
+                                   make_int4((int)w[4 * q], (int)w[4 * q + 1], (int)w[4 * q + 2], (int)w[4 * q + 3]));
                     }
                 }
             }
