@@ -106,7 +106,8 @@ size_t stage_bytes(int hg, bool box) {
 
 // + 1024: the box path aligns the stage ring to 1024 bytes (128-byte swizzle atoms)
 size_t decode_smem_bytes(int hg, int stages, bool box) {
-    return 1024 + stages * stage_bytes(hg, box) + stages * sizeof(TileMeta) + 2 * stages * sizeof(uint64_t) + 16;
+    return 1024 + stages * stage_bytes(hg, box) + stages * sizeof(TileMeta) + (2 * stages + 1) * sizeof(uint64_t) +
+           16;
 }
 
 template <bool kBox>
@@ -123,7 +124,8 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
     TileMeta *meta = reinterpret_cast<TileMeta *>(smem + (size_t)S * sbytes);
     uint64_t *full = reinterpret_cast<uint64_t *>(meta + S);
     uint64_t *empty = full + S;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + S);
+    uint64_t *patch = empty + S;   // box path, append mode: the current token's tile lands here first
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(patch + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g0 = blockIdx.y * hg;   // first kv head of this CTA
@@ -135,6 +137,7 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
             ptx::mbar_init(ptx::smem_u32(full + s), 1);
             ptx::mbar_init(ptx::smem_u32(empty + s), hg);
         }
+        ptx::mbar_init(ptx::smem_u32(patch), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -155,6 +158,8 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
         const long long r0 = per * blockIdx.x;
         const long long r1 = min(total, r0 + per);
         int it = 0;
+        uint32_t patch_uses = 0;
+        bool patch_pending = false;
         bool aborted = false;
         const uint32_t row_bytes = (uint32_t)hg * 256;
         // every K/V byte is read once: evict-first keeps the stream from displacing other lines
@@ -219,15 +224,69 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
                                 md.flags = (t0 == tlo ? kFirst : 0) | (t1 >= hi ? kLast : 0) | (ok ? 0 : kBad);
                                 md.mask = ok ? keys : 0u;
                                 if (!ok) report(a.status, MSGL_DEVERR_PAGE_RANGE);
-                                ptx::mbar_arrive_expect_tx(full_bar, ok ? (uint32_t)sbytes : 0u);
+                                // append mode: the tile holding the current token lands on the
+                                // patch barrier; its row is overwritten below before the stage
+                                // is handed over
+                                const bool patch_tile = a.new_loc != nullptr && hi == sb && sb - 1 < t1;
+                                const uint32_t land_bar = patch_tile ? ptx::smem_u32(patch) : full_bar;
+                                ptx::mbar_arrive_expect_tx(land_bar, ok ? (uint32_t)sbytes : 0u);
                                 if (ok) {
                                     const int slot0 = (pid_cur << a.pool.log2_ps) + (t0 & ((1 << a.pool.log2_ps) - 1));
                                     const uint32_t dst = ptx::smem_u32(smem + (size_t)stage * sbytes);
-                                    ptx::tma_load_3d_hint(dst, &k_map, 0, slot0, g0, full_bar, stream_policy);
-                                    ptx::tma_load_3d_hint(dst + half_bytes, &k_map, 64, slot0, g0, full_bar, stream_policy);
-                                    ptx::tma_load_3d_hint(dst + 2 * half_bytes, &v_map, 0, slot0, g0, full_bar, stream_policy);
-                                    ptx::tma_load_3d_hint(dst + 3 * half_bytes, &v_map, 64, slot0, g0, full_bar, stream_policy);
+                                    ptx::tma_load_3d_hint(dst, &k_map, 0, slot0, g0, land_bar, stream_policy);
+                                    ptx::tma_load_3d_hint(dst + half_bytes, &k_map, 64, slot0, g0, land_bar, stream_policy);
+                                    ptx::tma_load_3d_hint(dst + 2 * half_bytes, &v_map, 0, slot0, g0, land_bar, stream_policy);
+                                    ptx::tma_load_3d_hint(dst + 3 * half_bytes, &v_map, 64, slot0, g0, land_bar, stream_policy);
                                 }
+                            }
+                            // (only the CTA whose range ends at key sb - 1 handles it)
+                            if (a.new_loc != nullptr && hi == sb && sb - 1 < t1) {
+                                // current token (key sb - 1): its K/V come from k_new / v_new.  Wait for
+                                // the tile, write the token's rows of every head over the loaded ones
+                                // (swizzled positions), store them into the pool at new_loc[b], then
+                                // release the stage.
+                                const bool page_ok = __shfl_sync(0xffffffffu, pid_cur, 0) >= 0 &&
+                                                     __shfl_sync(0xffffffffu, pid_cur, 0) < a.pool.num_pages;
+                                if (!ptx::mbar_wait(ptx::smem_u32(patch), patch_uses & 1)) {
+                                    if (lane == 0) { report(a.status, MSGL_DEVERR_TIMEOUT); *abort_flag = 1; }
+                                    patch_pending = true;
+                                    aborted = true;
+                                    break;
+                                }
+                                ++patch_uses;
+                                const int kl = sb - 1 - t0;
+                                const long long src = (long long)b * slot_elems + (long long)g0 * kHeadDim;
+                                uint8_t *stage_p = smem + (size_t)stage * sbytes;
+                                for (int x = lane; x < hg * 16; x += 32) {
+                                    // x = (head, 16-byte chunk of the 128 dims)
+                                    const int h = x >> 4, c16 = x & 15;
+                                    const int hf = c16 >> 3, c = c16 & 7;
+                                    const uint32_t off = (uint32_t)(hf * half_bytes + (h * kTileKeys + kl) * 128 +
+                                                                    ((c ^ (kl & 7)) << 4));
+                                    const uint4 kv = ld_stream_16(a.k_new + src + h * kHeadDim + 8 * c16);
+                                    const uint4 vv = ld_stream_16(a.v_new + src + h * kHeadDim + 8 * c16);
+                                    *reinterpret_cast<uint4 *>(stage_p + off) = kv;
+                                    *reinterpret_cast<uint4 *>(stage_p + 2 * half_bytes + off) = vv;
+                                }
+                                const long long loc = __ldg(a.new_loc + b);
+                                const long long page_slot =
+                                    page_ok ? ((long long)__shfl_sync(0xffffffffu, pid_cur, 0) << a.pool.log2_ps) +
+                                                  ((sb - 1) & ((1 << a.pool.log2_ps) - 1))
+                                            : -1;
+                                if (loc < 0 || loc >= a.pool.num_slots) {
+                                    if (lane == 0) report(a.status, MSGL_DEVERR_SLOT_RANGE);
+                                } else {
+                                    if (lane == 0 && loc != page_slot) report(a.status, MSGL_DEVERR_APPEND_SLOT);
+                                    const long long dst = loc * slot_elems + (long long)g0 * kHeadDim;
+                                    for (int c = lane; c < hg * kHeadDim / 8; c += 32) {
+                                        const uint4 kv = ld_stream_16(a.k_new + src + 8 * c);
+                                        const uint4 vv = ld_stream_16(a.v_new + src + 8 * c);
+                                        *reinterpret_cast<uint4 *>(const_cast<__nv_bfloat16 *>(a.pool.k) + dst + 8 * c) = kv;
+                                        *reinterpret_cast<uint4 *>(const_cast<__nv_bfloat16 *>(a.pool.v) + dst + 8 * c) = vv;
+                                    }
+                                }
+                                __syncwarp();
+                                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(full + stage));
                             }
                             pid_cur = pid_next;
                             __syncwarp();
@@ -327,6 +386,7 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
             const int first = it > S ? it - S : 0;
             for (int k = first; k < it; ++k)
                 ptx::mbar_wait(ptx::smem_u32(full + (k % S)), (k / S) & 1, 200000000LL);
+            if (patch_pending) ptx::mbar_wait(ptx::smem_u32(patch), patch_uses & 1, 200000000LL);
         }
     } else if (warp < hg) {
         // ----------------------------------------------------------- consumers
@@ -692,7 +752,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     // tensor maps view each pool as [kv head][slot][128 dims] (innermost last), so a box
     // lands head-major: 16 consecutive keys of one head form 16 consecutive smem rows.
     const int hg = hkv <= kMaxHeadGroup ? hkv : kMaxHeadGroup;
-    bool box = a.new_loc == nullptr && (1 << a.pool.log2_ps) >= kTileKeys && a.pool.num_slots < INT_MAX;
+    bool box = (1 << a.pool.log2_ps) >= kTileKeys && a.pool.num_slots < INT_MAX;
     CUtensorMap km, vm;
     memset(&km, 0, sizeof km);
     memset(&vm, 0, sizeof vm);

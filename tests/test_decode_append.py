@@ -58,10 +58,26 @@ def test_append_short_and_page_boundary_lengths(ps):
     assert torch.equal(w.k_pool.view(torch.int16), full_k.view(torch.int16))
 
 
-def test_append_wrong_slot_is_flagged():
-    w = W.make_workload("appbad", 16, 8, 128, 1, seed=70, decode_seq_lens=[40, 50], device="cuda")
+@pytest.mark.parametrize("ps", [1, 64])
+def test_append_wrong_slot_is_flagged(ps):
+    w = W.make_workload("appbad", 16, 8, 128, ps, seed=70, decode_seq_lens=[40, 50], device="cuda")
     loc = w.decode.new_loc.clone()
     loc[1] = (int(loc[1]) + 1) % w.num_slots
     status = ops.new_status()
     _run(w, poison=False, loc=loc, status=status)
     assert ops.read_status(status) & ops.DEVERR_APPEND_SLOT
+
+
+def test_append_two_head_groups_and_split_requests():
+    """16 kv heads (two head groups per key) and requests long enough to span several CTA
+    ranges: only the range holding the current token writes it."""
+    w = W.make_workload("app16", 32, 16, 128, 64, seed=71, decode_seq_lens=[9000, 7000, 65, 3000],
+                        device="cuda")
+    o, lse, full_k, full_v = _run(w)
+    d = w.decode
+    ref_o, ref_l = oracle.decode(d.q.cpu(), full_k.cpu(), full_v.cpu(), w.page_size, d.page_table.cpu(),
+                                 d.seq_lens.cpu(), w.scale)
+    assert_o_close(o, ref_o, rounding_aware=True)
+    assert_lse_close(lse, ref_l)
+    assert torch.equal(w.k_pool.view(torch.int16), full_k.view(torch.int16))
+    assert torch.equal(w.v_pool.view(torch.int16), full_v.view(torch.int16))
