@@ -21,10 +21,14 @@
 //     keys x the group's heads (128-byte swizzle, head-major rows).  Four
 //     copies per stage: a TMA unit issues about one copy per 80 cycles, which
 //     held per-key copies near 50 GB/s per SM.
-//   - page_size < 16, or the append mode: each key's pool row (the group's
-//     heads, contiguous in the slot-major pool) arrives in one cp.async.bulk
-//     for K and one for V, at a pitch of row + 16 bytes so that ldmatrix over
-//     8 consecutive keys is free of bank conflicts.
+//     In the append mode the tile holding the current token lands on a
+//     separate barrier, and the producer writes that key's rows from
+//     k_new / v_new over the loaded ones before handing the stage over.
+//   - page_size < 16: each key's pool row (the group's heads, contiguous in
+//     the slot-major pool) arrives in one cp.async.bulk for K and one for V,
+//     at a pitch of row + 16 bytes so that ldmatrix over 8 consecutive keys is
+//     free of bank conflicts; in the append mode the current token's copies
+//     read k_new / v_new instead.
 // * One consumer warp per kv head computes S^T = K Q^T with m16n8k16 MMAs
 //   (M = 16 keys, N = the group's 8 q-head slots, K = 128 dims), keeps a
 //   base-2 online softmax per q head, transposes P to the B operand with
