@@ -469,20 +469,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < 16; ++q)
                         w[q] = ptx::pack_bf16(__uint_as_float(v[2 * q]) * inv, __uint_as_float(v[2 * q + 1]) * inv);
+                    // default L2 priority: the decode that follows reads its stream evict-first,
+                    // so these lines outlive that stream and are written back during
+                    // compute-bound work rather than in the middle of the decode
                     if (o_aligned32) {
-                        // 32-byte streaming stores: half the store instructions of 16-byte ones
-                        ptx::st_cs_v8(dst, w);
-                        ptx::st_cs_v8(dst + 16, w + 8);
+                        // 32-byte stores: half the store instructions of 16-byte ones
+                        ptx::st_v8(dst, w);
+                        ptx::st_v8(dst + 16, w + 8);
                     } else {
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
-                            __stcs(reinterpret_cast<int4 *>(dst) + q,
-                                   make_int4((int)w[4 * q], (int)w[4 * q + 1], (int)w[4 * q + 2], (int)w[4 * q + 3]));
+                            reinterpret_cast<uint4 *>(dst)[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
                     }
                 }
             }
             if (store) {
-                __stcs(a.lse + orow, (m_ref + log2f(l)) * kLn2);
+                a.lse[orow] = (m_ref + log2f(l)) * kLn2;
                 if (a.positions && jh == 0 && __ldg(a.positions + tok_g) != limit)
                     report(a.status, MSGL_DEVERR_POSITION);
             }

@@ -161,9 +161,9 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int 
         : "memory");
 }
 
-// 32-byte streaming store of eight 32-bit words (address 32-byte aligned).
-__device__ __forceinline__ void st_cs_v8(void *p, const uint32_t *w) {
-    asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+// 32-byte store of eight 32-bit words (address 32-byte aligned).
+__device__ __forceinline__ void st_v8(void *p, const uint32_t *w) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
                  "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
                  : "memory");
 }
