@@ -19,7 +19,7 @@
  *
  * Definitions used by every call (the pages fix no formula; this is the
  * plain reading of causal softmax attention with grouped heads):
- *   G        = num_q_heads / num_kv_heads; q head h reads kv head h / G
+ *   G        = num_q_heads / num_kv_heads (1..64); q head h reads kv head h / G
  *   slot(j)  = page_table[b][j / page_size] * page_size + j % page_size
  *   a query row at absolute position p attends keys j = 0..p:
  *   s_j = scale * <q, K[slot(j)][h/G]>,  o = sum_j softmax(s)_j V[slot(j)][h/G],
@@ -62,7 +62,7 @@ typedef struct CUstream_st *msgl_stream_t;
 typedef enum msgl_status {
     MSGL_OK = 0,
     MSGL_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or scalar */
-    MSGL_ERR_UNSUPPORTED = 2,   /* valid but not implemented (head_dim != 128, ...) */
+    MSGL_ERR_UNSUPPORTED = 2,   /* valid but not implemented (head_dim != 128, G > 64, ...) */
     MSGL_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed (launch, copy) */
     MSGL_ERR_OUT_OF_RANGE = 4,  /* reported by msgl_read_status: device index error */
     MSGL_ERR_TIMEOUT = 5,       /* reported by msgl_read_status: a bounded wait gave up */

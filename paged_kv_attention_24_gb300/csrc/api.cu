@@ -108,8 +108,6 @@ static msgl_status decode_impl(const msgl_kv_pool *pool, const msgl_page_table *
     if (max_seq_len <= 0) return fail(MSGL_ERR_INVALID_ARG, "max_seq_len must be > 0");
     if (!q || !seq_lens || !o || !lse) return fail(MSGL_ERR_INVALID_ARG, "q, seq_lens, o and lse must be non-NULL");
     if (!aligned16(q) || !aligned16(o)) return fail(MSGL_ERR_INVALID_ARG, "q and o must be 16-byte aligned");
-    if (pool->num_kv_heads > 8 && pool->num_kv_heads % 8 != 0)
-        return fail(MSGL_ERR_UNSUPPORTED, "decode needs num_kv_heads <= 8 or a multiple of 8");
     const msgl::DecodePlan plan = msgl::plan_decode(num_reqs, num_q_heads, pool->num_kv_heads, max_seq_len);
     if (!workspace || workspace_bytes < plan.workspace)
         return fail(MSGL_ERR_WORKSPACE, "decode needs %zu workspace bytes, got %zu", plan.workspace,

@@ -10,7 +10,7 @@
 namespace msgl {
 
 constexpr int kHeadDim = 128;          // the only head_dim the kernels are built for
-constexpr int kMaxGroup = 8;           // largest q-heads-per-kv-head ratio supported
+constexpr int kMaxGroup = 64;          // largest q-heads-per-kv-head ratio supported
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

@@ -69,6 +69,7 @@ struct DecodeKernelArgs {
     const __nv_bfloat16 *q;
     const int32_t *seq_lens;
     int32_t num_reqs, hq, group, max_seq_len, hg, stages;
+    int32_t slices;   // consumer warps per kv head: each takes 8 of its G q heads
     float scale_log2;
     float *part_o;
     float *part_lse;
@@ -139,7 +140,7 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(ptx::smem_u32(full + s), 1);
-            ptx::mbar_init(ptx::smem_u32(empty + s), hg);
+            ptx::mbar_init(ptx::smem_u32(empty + s), hg * a.slices);
         }
         ptx::mbar_init(ptx::smem_u32(patch), 1);
         *abort_flag = 0;
@@ -147,7 +148,8 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
     }
     __syncthreads();
 
-    if (warp == hg) {
+    const int n_consumers = hg * a.slices;
+    if (warp == n_consumers) {
         // ------------------------------------------------------------ producer
         const int B = a.num_reqs;
         long long total = 0;
@@ -392,10 +394,13 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
                 ptx::mbar_wait(ptx::smem_u32(full + (k % S)), (k / S) & 1, 200000000LL);
             if (patch_pending) ptx::mbar_wait(ptx::smem_u32(patch), patch_uses & 1, 200000000LL);
         }
-    } else if (warp < hg) {
+    } else if (warp < n_consumers) {
         // ----------------------------------------------------------- consumers
-        const int g = g0 + warp;                 // this warp's kv head
+        const int kvh = warp / a.slices;         // this warp's kv head within the group
+        const int g = g0 + kvh;
+        const int hoff = (warp - kvh * a.slices) * 8;   // its 8 q heads start at g * G + hoff
         const int G = a.group;
+        const int Gs = G - hoff;                 // q heads from hoff on (slots >= Gs are empty)
         const int qh = lane >> 2;                // q-head slot this lane loads for Q^T
         const int h0 = 2 * (lane & 3), h1 = h0 + 1;
         const int k0 = lane >> 2, k1 = k0 + 8;   // keys of this lane's S^T elements
@@ -410,13 +415,13 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
         const int kcol = 8 * (lane >> 4);
         const int vrow = (lane & 7) + 8 * (lane >> 4);
         const int vcol = 8 * ((lane >> 3) & 1);
-        const uint32_t k_lane = (uint32_t)(krow * pitch + warp * 256 + kcol * 2);
-        const uint32_t v_lane = (uint32_t)(kTileKeys * pitch + vrow * pitch + warp * 256 + vcol * 2);
+        const uint32_t k_lane = (uint32_t)(krow * pitch + kvh * 256 + kcol * 2);
+        const uint32_t v_lane = (uint32_t)(kTileKeys * pitch + vrow * pitch + kvh * 256 + vcol * 2);
         // Box path: row (head w, key k) of a 64-dim half sits at (16 w + k) * 128 bytes, its
         // 16-byte chunk c at position c ^ (k & 7) (k & 7 = lane & 7 for every ldmatrix row
         // this lane addresses).  Offset of dims [d, d + 8) of this lane's K / V row:
         auto box_off = [&](int row, int d) -> uint32_t {
-            return (uint32_t)((d >> 6) * half_bytes + (warp * kTileKeys + row) * 128 +
+            return (uint32_t)((d >> 6) * half_bytes + (kvh * kTileKeys + row) * 128 +
                               ((((d & 63) >> 3) ^ (lane & 7)) << 4));
         };
 
@@ -434,10 +439,10 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
             const uint32_t mask = meta[stage].mask;
 
             if (flags & kFirst) {
-                const __nv_bfloat16 *qp = a.q + ((long long)b * a.hq + (long long)g * G + qh) * kHeadDim;
+                const __nv_bfloat16 *qp = a.q + ((long long)b * a.hq + (long long)g * G + hoff + qh) * kHeadDim;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    if (qh < G) {
+                    if (qh < Gs) {
                         qf[ks][0] = *reinterpret_cast<const uint32_t *>(qp + 16 * ks + 2 * (lane & 3));
                         qf[ks][1] = *reinterpret_cast<const uint32_t *>(qp + 16 * ks + 8 + 2 * (lane & 3));
                     } else {
@@ -535,25 +540,25 @@ __global__ void __launch_bounds__(32 * (kMaxHeadGroup + 1), 1)
                 }
                 const float inv0 = lt0 > 0.f ? 1.f / lt0 : 0.f;
                 const float inv1 = lt1 > 0.f ? 1.f / lt1 : 0.f;
-                const long long hb = (long long)pslot * a.hq + (long long)g * G;
+                const long long hb = (long long)pslot * a.hq + (long long)g * G + hoff;
                 float *po = a.part_o + hb * kHeadDim;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int d0 = 16 * i + (lane >> 2), d1 = d0 + 8;
-                    if (h0 < G) {
+                    if (h0 < Gs) {
                         po[h0 * kHeadDim + d0] = acc[i][0] * inv0;
                         po[h0 * kHeadDim + d1] = acc[i][2] * inv0;
                     }
-                    if (h1 < G) {
+                    if (h1 < Gs) {
                         po[h1 * kHeadDim + d0] = acc[i][1] * inv1;
                         po[h1 * kHeadDim + d1] = acc[i][3] * inv1;
                     }
                 }
                 if (lane < 4) {
                     const float nan = __int_as_float(0x7fc00000);
-                    if (h0 < G)
+                    if (h0 < Gs)
                         a.part_lse[hb + h0] = (seg_bad || !(lt0 > 0.f)) ? nan : (m2[0] + log2f(lt0)) * kLn2;
-                    if (h1 < G)
+                    if (h1 < Gs)
                         a.part_lse[hb + h1] = (seg_bad || !(lt1 > 0.f)) ? nan : (m2[1] + log2f(lt1)) * kLn2;
                 }
             }
@@ -713,9 +718,20 @@ struct Launch {
     size_t smem;
 };
 
-Launch decode_launch_shape(int hkv, bool box) {
+// Consumer warps per kv head: each covers 8 of its G q heads (the N = 8 MMA slots).
+int decode_slices(int group) { return (group + 7) / 8; }
+
+// kv heads per CTA: the largest divisor of hkv whose consumer warps (hg x slices) fit in 8.
+int decode_head_group(int hkv, int slices) {
+    int hg = kMaxHeadGroup / slices;
+    if (hg < 1) hg = 1;
+    while (hkv % hg) --hg;
+    return hg;
+}
+
+Launch decode_launch_shape(int hkv, int slices, bool box) {
     Launch L;
-    L.hg = hkv <= kMaxHeadGroup ? hkv : kMaxHeadGroup;
+    L.hg = decode_head_group(hkv, slices);
     int st = (int)((kSmemBudget - 1024 - 64) / (stage_bytes(L.hg, box) + sizeof(TileMeta) + 16));
     L.stages = st < 2 ? 2 : (st > kMaxStages ? kMaxStages : st);
     L.smem = decode_smem_bytes(L.hg, L.stages, box);
@@ -751,11 +767,12 @@ DecodePlan plan_decode(int32_t num_reqs, int32_t hq, int32_t hkv, int32_t max_se
 cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream) {
     if (a.num_reqs == 0) return cudaSuccess;
     const int hkv = a.pool.hkv;
-    if (hkv > kMaxHeadGroup && hkv % kMaxHeadGroup != 0) return cudaErrorInvalidValue;
+    const int slices = decode_slices(a.hq / hkv);
+    if (slices > kMaxHeadGroup) return cudaErrorInvalidValue;   // G > 64
     // Box path: whole 16-key tiles by 3D TMA (page_size >= 16, not the append mode).  Its
     // tensor maps view each pool as [kv head][slot][128 dims] (innermost last), so a box
     // lands head-major: 16 consecutive keys of one head form 16 consecutive smem rows.
-    const int hg = hkv <= kMaxHeadGroup ? hkv : kMaxHeadGroup;
+    const int hg = decode_head_group(hkv, slices);
     bool box = (1 << a.pool.log2_ps) >= kTileKeys && a.pool.num_slots < INT_MAX;
     CUtensorMap km, vm;
     memset(&km, 0, sizeof km);
@@ -775,7 +792,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
                 return cudaErrorInvalidValue;
         }
     }
-    const Launch L = decode_launch_shape(hkv, box);
+    const Launch L = decode_launch_shape(hkv, slices, box);
     static bool attr_set[64];   // per device; idempotent, racing setters write the same value
     int dev = 0;
     cudaGetDevice(&dev);
@@ -798,6 +815,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     k.group = a.hq / hkv;
     k.max_seq_len = a.max_seq_len;
     k.hg = L.hg;
+    k.slices = slices;
     k.stages = L.stages;
     k.scale_log2 = a.scale * kLog2e;
     k.part_o = a.part_o;
@@ -810,9 +828,9 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     if (L.smem > (size_t)kSmemBudget) return cudaErrorInvalidValue;
     dim3 grid(L.ctas, hkv / L.hg);
     if (box)
-        decode_split_kernel<true><<<grid, 32 * (L.hg + 1), L.smem, stream>>>(km, vm, k);
+        decode_split_kernel<true><<<grid, 32 * (L.hg * slices + 1), L.smem, stream>>>(km, vm, k);
     else
-        decode_split_kernel<false><<<grid, 32 * (L.hg + 1), L.smem, stream>>>(km, vm, k);
+        decode_split_kernel<false><<<grid, 32 * (L.hg * slices + 1), L.smem, stream>>>(km, vm, k);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // programmatic dependent launch: the merge's launch and its seq_lens scan overlap the

@@ -78,8 +78,8 @@ def test_host_validation_needs_no_gpu(lib):
     rc = lib.msgl_attn_decode(ctypes.byref(pool), ctypes.byref(pages), 16, 16, 16, 1, 10, -1.0, 16, 16,
                               None, 0, None, None)
     assert rc == 1
-    # more than 8 q heads per kv head is unsupported
-    rc = lib.msgl_attn_decode(ctypes.byref(pool), ctypes.byref(pages), 16, 128, 16, 1, 10, 0.1, 16, 16,
+    # more than 64 q heads per kv head is unsupported (8 kv heads here)
+    rc = lib.msgl_attn_decode(ctypes.byref(pool), ctypes.byref(pages), 16, 8 * 72, 16, 1, 10, 0.1, 16, 16,
                               None, 0, None, None)
     assert rc == 2
     # a split decode without workspace

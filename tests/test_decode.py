@@ -54,6 +54,18 @@ def test_decode_shapes(ps, hq, hkv):
     assert_lse_close(lse, ref_l)
 
 
+@pytest.mark.parametrize("hq,hkv,ps", [(128, 8, 16), (32, 2, 1), (48, 2, 64), (64, 1, 16), (24, 12, 16), (12, 3, 1)])
+def test_decode_more_than_eight_q_heads_per_kv_head(hq, hkv, ps):
+    """G > 8 (several consumer warps per kv head, smaller head groups) and kv head counts that
+    are neither <= 8 nor multiples of 8."""
+    seqs = [1, 40, 333, 1500, 2049]
+    w = W.make_workload("wideg", hq, hkv, 128, ps, seed=hq * 7 + hkv + ps, decode_seq_lens=seqs, device="cuda")
+    o, lse = run_gpu(w)
+    ref_o, ref_l = run_oracle(w)
+    assert_o_close(o, ref_o, f"hq={hq} hkv={hkv} ps={ps}", rounding_aware=True)
+    assert_lse_close(lse, ref_l)
+
+
 def test_decode_long_single_request():
     """One 65k-token request: many key chunks merged by LSE."""
     w = W.make_workload("long", 16, 8, 128, 16, seed=3, decode_seq_lens=[65536], device="cuda")

@@ -168,6 +168,17 @@ def test_extend_group_and_page_variants(ps, hq, hkv):
     assert_lse_close(lse, ref_l)
 
 
+@pytest.mark.parametrize("hq,hkv,ps", [(128, 8, 16), (64, 2, 1), (64, 1, 64), (48, 3, 16)])
+def test_extend_more_than_eight_q_heads_per_kv_head(hq, hkv, ps):
+    """G = 16, 32, 64 (a 128-row Q tile holds 8, 4 or 2 tokens) and an odd kv head count."""
+    w = W.make_workload("wideg", hq, hkv, 128, ps, seed=hq + hkv + ps, extend_prefix_lens=[0, 37, 300],
+                        extend_ext_lens=[19, 130, 64], device="cuda")
+    o, lse = run_gpu(w)
+    ref_o, ref_l = run_oracle(w)
+    assert_o_close(o, ref_o, f"hq={hq} hkv={hkv} ps={ps}", rounding_aware=True)
+    assert_lse_close(lse, ref_l)
+
+
 @pytest.mark.parametrize("ext", [1, 2, 3, 7])
 def test_extend_chunk_smaller_than_tile(ext):
     """Fewer tokens than one Q tile holds (the TMA box is clipped to the tokens that exist)."""
