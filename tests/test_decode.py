@@ -66,6 +66,42 @@ def test_decode_more_than_eight_q_heads_per_kv_head(hq, hkv, ps):
     assert_lse_close(lse, ref_l)
 
 
+def test_decode_large_batch_graph_replay():
+    """A 192-request batch (split and merge under programmatic dependent launch) captured in a
+    CUDA graph and replayed with new lengths."""
+    seqs = [4000, 3500, 2900, 4096, 1200, 3900, 4096, 2500] * 24
+    w = W.make_workload("poolgraph", 40, 8, 128, 16, seed=23, decode_seq_lens=seqs, device="cuda")
+    d = w.decode
+    pool = ops.KVPool(w.k_pool, w.v_pool, 16)
+    ws = torch.empty(ops.decode_workspace_size(d.num_reqs, w.hq, w.hkv, 4096), dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(d.q)
+    lse = torch.empty(d.q.shape[:2], dtype=torch.float32, device="cuda")
+    status = ops.new_status()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        ops.attn_decode(pool, d.q, d.page_table, d.seq_lens, 4096, w.scale, out=o, lse=lse, workspace=ws,
+                        status=status)
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        ops.attn_decode(pool, d.q, d.page_table, d.seq_lens, 4096, w.scale, out=o, lse=lse, workspace=ws,
+                        status=status)
+    full = d.seq_lens.clone()
+    for trial in range(2):
+        # new lengths within each request's pages
+        frac = torch.rand(full.shape, device="cuda")
+        d.seq_lens.copy_(torch.clamp((full.float() * frac).to(torch.int32), min=1))
+        o.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert ops.read_status(status) == 0
+        rows = list(range(0, d.num_reqs, 17)) + [d.num_reqs - 1]
+        ref_o, ref_l = run_oracle(w, rows)
+        assert_o_close(o[rows], ref_o, f"replay {trial}")
+        assert_lse_close(lse[rows], ref_l)
+
+
 def test_decode_long_single_request():
     """One 65k-token request: many key chunks merged by LSE."""
     w = W.make_workload("long", 16, 8, 128, 16, seed=3, decode_seq_lens=[65536], device="cuda")
