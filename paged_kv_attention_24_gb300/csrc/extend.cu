@@ -469,9 +469,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < 16; ++q)
                         w[q] = ptx::pack_bf16(__uint_as_float(v[2 * q]) * inv, __uint_as_float(v[2 * q + 1]) * inv);
-                    // default L2 priority: the decode that follows reads its stream evict-first,
-                    // so these lines outlive that stream and are written back during
-                    // compute-bound work rather than in the middle of the decode
                     if (o_aligned32) {
                         // 32-byte stores: half the store instructions of 16-byte ones
                         ptx::st_v8(dst, w);
