@@ -224,7 +224,8 @@ def oracle_sample(w, cpu_seconds, n_threads):
         q, pt = e.q.cpu(), e.page_table.cpu()
         cu, pre = e.cu_ext.cpu().numpy(), e.prefix_lens.cpu().numpy()
         rng = np.random.default_rng(0)
-        while ext_time < budget and ext_rows < e.total_tokens:
+        ext_budget = cpu_seconds - dec_time   # what the decode sample left over
+        while ext_time < ext_budget and ext_rows < e.total_tokens:
             toks = rng.integers(0, e.total_tokens, size=max(1, n_threads // 2)).astype(np.int32)
             r_of = np.searchsorted(cu, toks, side="right") - 1
             pos = pre[r_of] + toks - cu[r_of]
