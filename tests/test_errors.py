@@ -3,12 +3,13 @@
 Device-side cases use in-bounds buffers only; the bad value is an index the
 kernel range-checks before any access, so nothing out of bounds is read.
 """
+import numpy as np
 import pytest
 import torch
 
 from paged_kv_attention_24_gb300 import ops
 from paged_kv_attention_24_gb300 import workloads as W
-from tests.parity import assert_o_close
+from tests.parity import assert_lse_close, assert_o_close
 
 pytestmark = pytest.mark.gpu
 
@@ -158,3 +159,19 @@ def test_bounded_wait_times_out_into_status_and_context_survives():
     ref_o, _ = oracle.decode(d.q.cpu(), w.k_pool.cpu(), w.v_pool.cpu(), 16, d.page_table.cpu(),
                              d.seq_lens.cpu(), w.scale)
     assert_o_close(o, ref_o)
+
+
+def test_extend_chunk_longer_than_max_ext_len_is_a_length_error():
+    """A chunk longer than the max_ext_len bound: status bit set; the other request's rows exact."""
+    from tests.test_extend import run_oracle
+    w = W.make_workload("ext_over", 16, 8, 128, 16, seed=8, extend_prefix_lens=[100, 40],
+                        extend_ext_lens=[50, 300], device="cuda")
+    e = w.extend
+    status = ops.new_status()
+    o, lse = ops.attn_extend(ops.KVPool(w.k_pool, w.v_pool, w.page_size), e.q, e.page_table, e.prefix_lens,
+                             e.ext_lens, e.cu_ext, 60, e.max_seq_len, w.scale, status=status)
+    assert ops.read_status(status) & ops.DEVERR_LENGTH
+    rows = np.arange(50, dtype=np.int32)
+    ref_o, ref_l = run_oracle(w, rows)
+    assert_o_close(o[:50], ref_o, "in-bound request")
+    assert_lse_close(lse[:50], ref_l, "in-bound request")
