@@ -269,3 +269,42 @@ def test_shared_prefix_page_tables_match_private_pages():
         np.testing.assert_allclose(lse, lse2, rtol=0, atol=1e-12)
         c.insert(toks, pages, lease)               # finished: cache its full pages
     assert prefixes == [0, 12, 8, 12]
+
+
+def test_eviction_cost_follows_pages_freed_not_tree_size():
+    """A full 1M-page pool: evicting allocations cost per page freed, not per cached page.
+
+    1024 cached chains of 1024 single-token pages fill the pool.  Two hundred 1-page
+    allocations (each evicts one leaf) and then one 100k-page allocation must be fast;
+    a walk of the whole tree per allocation would take seconds for the first part alone.
+    Eviction order stays oldest-first: the first chains inserted lose their tails first.
+    """
+    import time
+    n_chain, chain = 1024, 1024
+    c = RadixCache(page_size=1, num_pages=n_chain * chain)
+    for i in range(n_chain):
+        toks = np.arange(chain, dtype=np.int32) + i * chain
+        _, _, lease = c.match(toks)
+        c.insert(toks, c.alloc(chain), lease)
+    assert c.stats() == {"free": 0, "cached": n_chain * chain, "pinned": 0}
+    t0 = time.perf_counter()
+    for _ in range(200):
+        c.alloc(1)
+    t_small = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    c.alloc(100_000)
+    t_big = time.perf_counter() - t0
+    assert t_small < 0.5, f"200 one-page evictions took {t_small:.2f} s"
+    assert t_big < 2.0, f"a 100k-page eviction took {t_big:.2f} s"
+    assert c.stats()["cached"] == n_chain * chain - 100_200
+    # 100,200 = 97 * 1024 + 872: chains 0..96 (the oldest) are gone, chain 97 lost its
+    # last 872 pages, chain 98 is whole
+    n, _, lease = c.match(np.arange(chain, dtype=np.int32) + 97 * chain)
+    assert n == chain - 872
+    c.release(lease, [])
+    n, _, lease = c.match(np.arange(chain, dtype=np.int32) + 98 * chain)
+    assert n == chain
+    c.release(lease, [])
+    n, _, lease = c.match(np.arange(chain, dtype=np.int32))
+    assert n == 0
+    c.release(lease, [])
