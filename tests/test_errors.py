@@ -171,7 +171,6 @@ def test_extend_chunk_longer_than_max_ext_len_is_a_length_error():
     o, lse = ops.attn_extend(ops.KVPool(w.k_pool, w.v_pool, w.page_size), e.q, e.page_table, e.prefix_lens,
                              e.ext_lens, e.cu_ext, 60, e.max_seq_len, w.scale, status=status)
     assert ops.read_status(status) & ops.DEVERR_LENGTH
-    rows = np.arange(50, dtype=np.int32)
-    ref_o, ref_l = run_oracle(w, rows)
-    assert_o_close(o[:50], ref_o, "in-bound request")
-    assert_lse_close(lse[:50], ref_l, "in-bound request")
+    ref_o, ref_l = run_oracle(w)
+    assert_o_close(o[:50], ref_o[:50], "in-bound request")
+    assert_lse_close(lse[:50], ref_l[:50], "in-bound request")

@@ -21,43 +21,16 @@ def run_gpu(w, status=None, q=None, prefix=None, ext=None, cu=None, positions=No
                            positions=e.positions if positions is None else positions, status=status)
 
 
-def run_oracle(w, tokens=None):
+def run_oracle(w, v_abs=False):
+    """The oracle's (o, lse); with v_abs, o over |V| (the rounding allowance's A)."""
     e = w.extend
-    kp, vp = w.k_pool.cpu(), w.v_pool.cpu()
-    if tokens is None:
-        return oracle.extend(e.q.cpu(), kp, vp, w.page_size, e.page_table.cpu(), e.prefix_lens.cpu(),
-                             e.ext_lens.cpu(), w.scale)
-    cu = e.cu_ext.cpu().numpy()
-    pre = e.prefix_lens.cpu().numpy()
-    tokens = np.asarray(tokens, dtype=np.int32)
-    req_of = np.searchsorted(cu, tokens, side="right") - 1
-    pos = pre[req_of] + (tokens - cu[req_of])
-    req = np.repeat(req_of, w.hq).astype(np.int32)
-    row = np.repeat(tokens, w.hq).astype(np.int32)
-    pp = np.repeat(pos, w.hq).astype(np.int32)
-    head = np.tile(np.arange(w.hq, dtype=np.int32), len(tokens))
-    o, lse = oracle.attention_items(e.q.cpu(), kp, vp, w.page_size, e.page_table.cpu(), w.scale,
-                                    req, row, pp, head)
-    return o.reshape(len(tokens), w.hq, w.d), lse.reshape(len(tokens), w.hq)
+    vp = w.v_pool.cpu()
+    return oracle.extend(e.q.cpu(), w.k_pool.cpu(), vp.abs() if v_abs else vp, w.page_size,
+                         e.page_table.cpu(), e.prefix_lens.cpu(), e.ext_lens.cpu(), w.scale)
 
 
-def sample_tokens(w, n_random=96, seed=0):
-    """First/last rows of every request, rows at tile boundaries, and random rows."""
-    e = w.extend
-    cu = e.cu_ext.cpu().numpy()
-    picks = set()
-    for b in range(len(cu) - 1):
-        lo, hi = int(cu[b]), int(cu[b + 1])
-        for t in (lo, lo + 1, hi - 2, hi - 1):
-            if lo <= t < hi:
-                picks.add(t)
-        for k in (16, 25, 64, 128, 256):
-            for t in (lo + k - 1, lo + k):
-                if lo <= t < hi:
-                    picks.add(t)
-    rng = np.random.default_rng(seed)
-    picks.update(rng.integers(0, int(cu[-1]), size=n_random).tolist())
-    return np.array(sorted(picks), dtype=np.int32)
+def abs_ref(w):
+    return run_oracle(w, v_abs=True)[0]
 
 
 def test_extend_config2_full():
@@ -71,18 +44,23 @@ def test_extend_config2_full():
 
 
 @pytest.mark.parametrize("cfg", [4, 5])
-def test_extend_large_configs_sampled(cfg):
+def test_extend_large_configs_full(cfg):
+    """Every row and every q head of the Qwen3-14B and Qwen3-32B extends against the oracle.
+
+    Qwen3-14B: one 8192-token chunk over a 4096-token cached prefix (40/8 heads, page
+    size 16).  Qwen3-32B: 8 chunks of 1024 tokens over one shared 2048-token prefix
+    (64/8 heads, page size 64).  The oracle takes about 35 s and 18 s of fp64 work on
+    16 host cores.
+    """
     w = W.config(cfg, device="cuda", part="extend")
     status = ops.new_status()
     o, lse = run_gpu(w, status)
     assert ops.read_status(status) == 0
-    toks = sample_tokens(w, seed=cfg)
-    ref_o, ref_l = run_oracle(w, toks)
-    idx = torch.from_numpy(toks).long().cuda()
-    assert_o_close(o[idx], ref_o, f"config {cfg}")
-    assert_lse_close(lse[idx], ref_l, f"config {cfg}")
-    # every row finite, and every row's LSE at least the log of its key count minus a margin
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    ref_o, ref_l = run_oracle(w)
+    assert ref_o.shape == tuple(o.shape) and ref_l.shape == tuple(lse.shape)
+    assert_o_close(o, ref_o, f"config {cfg}")
+    assert_lse_close(lse, ref_l, f"config {cfg}")
 
 
 @pytest.mark.parametrize("ps", [1, 16, 64, 256])
@@ -94,7 +72,7 @@ def test_extend_ragged_shapes(ps, hq, hkv):
                         extend_ext_lens=ext, device="cuda")
     o, lse = run_gpu(w)
     ref_o, ref_l = run_oracle(w)
-    assert_o_close(o, ref_o, f"ps={ps} hq={hq}", rounding_aware=True)
+    assert_o_close(o, ref_o, f"ps={ps} hq={hq}", abs_ref=abs_ref(w))
     assert_lse_close(lse, ref_l)
 
 
@@ -104,7 +82,7 @@ def test_extend_shared_prefix_pages():
                         extend_ext_lens=[200, 64, 1, 333], shared_prefix_len=512, device="cuda")
     o, lse = run_gpu(w)
     ref_o, ref_l = run_oracle(w)
-    assert_o_close(o, ref_o, rounding_aware=True)
+    assert_o_close(o, ref_o, abs_ref=abs_ref(w))
     assert_lse_close(lse, ref_l)
 
 
@@ -124,7 +102,7 @@ def test_chunked_equals_unchunked_on_gpu():
         assert (o.float() - o_full[lo:hi].float()).abs().max().item() <= 1e-2
         assert (l - l_full[lo:hi]).abs().max().item() <= 1e-3
     ref_o, ref_l = run_oracle(w)
-    assert_o_close(o_full, ref_o, rounding_aware=True)
+    assert_o_close(o_full, ref_o, abs_ref=abs_ref(w))
 
 
 def test_decode_equals_last_extend_row():
@@ -148,7 +126,7 @@ def test_extend_without_positions():
     o, lse = ops.attn_extend(pool, e.q, e.page_table, e.prefix_lens, e.ext_lens, e.cu_ext,
                              e.max_ext_len, e.max_seq_len, w.scale, positions=None)
     ref_o, ref_l = run_oracle(w)
-    assert_o_close(o, ref_o, rounding_aware=True)
+    assert_o_close(o, ref_o, abs_ref=abs_ref(w))
     assert_lse_close(lse, ref_l)
 
 
@@ -164,7 +142,7 @@ def test_extend_group_and_page_variants(ps, hq, hkv):
     o, lse = run_gpu(w, status)
     assert ops.read_status(status) == 0
     ref_o, ref_l = run_oracle(w)
-    assert_o_close(o, ref_o, f"ps={ps} hq={hq}", rounding_aware=True)
+    assert_o_close(o, ref_o, f"ps={ps} hq={hq}", abs_ref=abs_ref(w))
     assert_lse_close(lse, ref_l)
 
 
@@ -175,7 +153,7 @@ def test_extend_more_than_eight_q_heads_per_kv_head(hq, hkv, ps):
                         extend_ext_lens=[19, 130, 64], device="cuda")
     o, lse = run_gpu(w)
     ref_o, ref_l = run_oracle(w)
-    assert_o_close(o, ref_o, f"hq={hq} hkv={hkv} ps={ps}", rounding_aware=True)
+    assert_o_close(o, ref_o, f"hq={hq} hkv={hkv} ps={ps}", abs_ref=abs_ref(w))
     assert_lse_close(lse, ref_l)
 
 
@@ -186,7 +164,7 @@ def test_extend_chunk_smaller_than_tile(ext):
                         extend_ext_lens=[ext], device="cuda")
     o, lse = run_gpu(w)
     ref_o, ref_l = run_oracle(w)
-    assert_o_close(o, ref_o, rounding_aware=True)
+    assert_o_close(o, ref_o, abs_ref=abs_ref(w))
     assert_lse_close(lse, ref_l)
 
 
@@ -196,7 +174,7 @@ def test_extend_long_prefix_many_tiles():
                         extend_ext_lens=[40, 200], device="cuda")
     o, lse = run_gpu(w)
     ref_o, ref_l = run_oracle(w)
-    assert_o_close(o, ref_o, rounding_aware=True)
+    assert_o_close(o, ref_o, abs_ref=abs_ref(w))
     assert_lse_close(lse, ref_l)
 
 
@@ -247,5 +225,5 @@ def test_extend_zero_length_requests_and_graph_replay(ps):
     graph.replay()
     torch.cuda.synchronize()
     ref_o, ref_l = run_oracle(w)
-    assert_o_close(o, ref_o, rounding_aware=True)
+    assert_o_close(o, ref_o, abs_ref=abs_ref(w))
     assert_lse_close(lse, ref_l)
