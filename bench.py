@@ -52,6 +52,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--no-append", action="store_true", help="skip the fused append+decode timing")
+    ap.add_argument("--no-mixed", action="store_true", help="skip the mixed-step (msgl_attn_mixed) timing")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-config legs (configs 2, 3 and 4) after the headline step")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="approximate CPU seconds for the oracle sample")
     return ap.parse_args(argv)
@@ -69,6 +72,17 @@ def load_peaks():
                 "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
             "source": "fallback"}
+
+
+def tensor_peak(peaks, region_ms):
+    """The bf16 peak a tensor-bound kernel is judged against, by the length of the timed region.
+
+    A region of a few seconds or more runs under the power cap (sustained figure);
+    a shorter one times the kernel in near-isolation (burst figure).
+    """
+    if region_ms >= 2000.0:
+        return "sustained", peaks["bf16_tflops_sustained"]
+    return "burst", peaks["bf16_tflops"]
 
 
 def kernel_source_sha(files):
@@ -391,9 +405,12 @@ def run_ours(args):
                                "traffic": recorded_traffic("decode", w.name),
                                "us_per_launch": dec_avg * 1e3}
     if e is not None:
-        pk = peaks["bf16_tflops_sustained"]
+        # a region under ~2 s is a kernel timed in near-isolation: the burst peak applies
+        kind, pk = tensor_peak(peaks, total_ms)
         rooflines["extend"] = {"bound": "tensor", "achieved": per_gpu_ext, "peak": pk,
-                               "unit": "TFLOP/s", "frac": per_gpu_ext / pk,
+                               "peak_kind": kind, "unit": "TFLOP/s", "frac": per_gpu_ext / pk,
+                               "frac_burst": per_gpu_ext / peaks["bf16_tflops"],
+                               "frac_sustained": per_gpu_ext / peaks["bf16_tflops_sustained"],
                                "traffic": recorded_traffic("extend", w.name),
                                "us_per_launch": ext_avg * 1e3}
     if st_gbs:
@@ -430,6 +447,11 @@ def run_ours(args):
     if not args.no_graph:
         graph = measure_graph(args, step, stream, total_ms / args.steps, dev)
 
+    mixed = None
+    if e is not None and d is not None and not args.no_mixed:
+        mixed = measure_mixed(args, w, pool, k_new, v_new, loc, status, stream, total_ms / args.steps,
+                              graph["ms_per_step"] if graph else None)
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         import oracle
@@ -437,6 +459,10 @@ def run_ours(args):
         r = oracle_sample(wc, args.cpu_seconds, oracle.default_threads())
         cpu = {"value": r["decode_gbs"], "unit": "GB/s", "cores": r["cores"], "kind": "oracle",
                "sample": r["sample"], "extend_tflops": r["extend_tflops"]}
+
+    extra = None
+    if not args.no_configs and ws == 1 and args.config == 5 and args.page_size is None:
+        extra = measure_other_configs(args, dev, peaks)
 
     if rank != 0:
         return 0
@@ -453,7 +479,11 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (decode KV %.2f GB per step), no flush" % (dec_bytes / 1e9),
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
         "extend": {"value": ext_tf, "unit": "TFLOP/s",
-                   "frac": (per_gpu_ext / peaks["bf16_tflops_sustained"]) if e else None},
+                   "frac": rooflines["extend"]["frac"] if e else None,
+                   "frac_burst": rooflines["extend"]["frac_burst"] if e else None,
+                   "frac_sustained": rooflines["extend"]["frac_sustained"] if e else None,
+                   "sm_mhz": clocks["sm_mhz"] if clocks else None,
+                   "kcycles_per_launch": (ext_avg * clocks["sm_mhz"]) if (e and clocks) else None},
         "store": {"value": st_gbs, "unit": "GB/s"},
         "roofline": dict(rooflines[dominant], kernel=dominant),
         "rooflines": rooflines,
@@ -463,12 +493,164 @@ def run_ours(args):
         "gpu_launches": launches_per_step * args.steps,
         "graph": graph,
         "decode_append": append,
+        "mixed": mixed,
+        "configs": extra,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+L2_FLUSH_BYTES = 2 * 129 * 1024 * 1024   # twice the GB300 L2
+
+
+def time_calls(call, n, flush=None):
+    """Mean device time (ms) of ``call`` over n launches, CUDA events on the current stream.
+
+    With ``flush`` (a uint8 buffer larger than L2), the buffer is rewritten between
+    launches, outside the events, so every timed launch starts with a cold L2.
+    """
+    import torch
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        call()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:
+        if flush is not None:
+            flush.fill_(1)
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+
+def measure_other_configs(args, dev, peaks):
+    """Decode and extend of the other throughput workloads, one call at a time.
+
+    offline decode (256 requests, page size 1), Qwen3-14B decode (128 requests, page
+    size 16) and extend (8192 tokens over a 4096 prefix), and the radix extend batch
+    (8 requests, page size 1).  Inputs smaller than twice the L2 are timed with the L2
+    flushed before every call.
+    """
+    import torch
+    from paged_kv_attention_24_gb300 import ops
+    from paged_kv_attention_24_gb300 import workloads as W
+    from paged_kv_attention_24_gb300 import accounting as A
+    n = max(20, min(args.steps, 200))
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    out = {}
+    status = ops.new_status(dev)
+    with ClockSampler(dev.index) as clk:
+        for cid, parts in ((3, ("decode",)), (4, ("decode", "extend")), (2, ("extend",))):
+            w = W.config(cid, device=dev)
+            pool = ops.KVPool(w.k_pool, w.v_pool, w.page_size)
+            entry = {"workload": w.name}
+            if "decode" in parts:
+                d = w.decode
+                o = torch.empty_like(d.q)
+                l = torch.empty(d.q.shape[:2], dtype=torch.float32, device=dev)
+                wsb = torch.empty(ops.decode_workspace_size(d.num_reqs, w.hq, w.hkv, d.max_seq_len),
+                                  dtype=torch.uint8, device=dev)
+                nbytes = A.decode_kv_bytes(w)
+                cold = nbytes < L2_FLUSH_BYTES
+                ms = time_calls(lambda: ops.attn_decode(pool, d.q, d.page_table, d.seq_lens, d.max_seq_len,
+                                                        w.scale, out=o, lse=l, workspace=wsb, status=status),
+                                n, flush if cold else None)
+                gbs = nbytes / (ms * 1e-3) / 1e9
+                entry["decode"] = {"value": gbs, "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                                   "us_per_call": ms * 1e3, "kv_bytes": nbytes,
+                                   "l2": "flushed before each call" if cold else "inputs larger than L2"}
+            if "extend" in parts:
+                e = w.extend
+                o = torch.empty_like(e.q)
+                l = torch.empty(e.q.shape[:2], dtype=torch.float32, device=dev)
+                flops = A.extend_flops(w)
+                ms = time_calls(lambda: ops.attn_extend(pool, e.q, e.page_table, e.prefix_lens, e.ext_lens,
+                                                        e.cu_ext, e.max_ext_len, e.max_seq_len, w.scale,
+                                                        positions=e.positions, out=o, lse=l, status=status),
+                                n, flush)
+                tf = flops / (ms * 1e-3) / 1e12
+                entry["extend"] = {"value": tf, "unit": "TFLOP/s", "frac_burst": tf / peaks["bf16_tflops"],
+                                   "frac_sustained": tf / peaks["bf16_tflops_sustained"],
+                                   "us_per_call": ms * 1e3, "flop": flops, "l2": "flushed before each call"}
+            out[str(cid)] = entry
+            del w, pool
+        torch.cuda.synchronize()
+    assert ops.read_status(status) == 0, "device status set in the per-config legs"
+    clocks = clk.summary()
+    for entry in out.values():
+        entry["clocks"] = clocks
+    out["calls_per_leg"] = n
+    return out
+
+
+def measure_mixed(args, w, pool, k_new, v_new, loc, status, stream, eager_ms, graph_ms):
+    """The same step with extend and decode in one msgl_attn_mixed call (store, then mixed).
+
+    Timed eagerly over the same number of steps as the headline and as a CUDA-graph
+    replay; the outputs are checked bit for bit against the separate calls first.
+    """
+    import torch
+    from paged_kv_attention_24_gb300 import ops
+    e, d = w.extend, w.decode
+    outs = [torch.empty_like(e.q), torch.empty(e.q.shape[:2], dtype=torch.float32, device=e.q.device),
+            torch.empty_like(d.q), torch.empty(d.q.shape[:2], dtype=torch.float32, device=d.q.device)]
+    ws = torch.empty(ops.mixed_workspace_size(d.num_reqs, e.total_tokens, e.num_reqs, w.hq, w.hkv,
+                                              e.max_seq_len, d.max_seq_len), dtype=torch.uint8,
+                     device=e.q.device)
+
+    def step():
+        ops.store_kv(pool, k_new, v_new, loc, status=status)
+        ops.attn_mixed(pool, w.scale, e.q, e.page_table, e.prefix_lens, e.ext_lens, e.cu_ext, e.max_ext_len,
+                       e.max_seq_len, d.q, d.page_table, d.seq_lens, d.max_seq_len, positions=e.positions,
+                       ext_out=outs[0], ext_lse=outs[1], dec_out=outs[2], dec_lse=outs[3], workspace=ws,
+                       status=status)
+
+    step()
+    oe, le = ops.attn_extend(pool, e.q, e.page_table, e.prefix_lens, e.ext_lens, e.cu_ext, e.max_ext_len,
+                             e.max_seq_len, w.scale, positions=e.positions)
+    od, ld = ops.attn_decode(pool, d.q, d.page_table, d.seq_lens, d.max_seq_len, w.scale)
+    same = all(torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32),
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b.view(torch.int32))
+               for a, b in zip(outs, (oe, le, od, ld)))
+    assert same, "mixed step differs from the separate calls"
+    n = max(20, min(args.steps, 500))
+    for _ in range(max(3, args.warmup)):
+        step()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(n):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    mixed_ms = t0.elapsed_time(t1) / n
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()
+    stream.wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(n):
+        g.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    graph_mixed_ms = t0.elapsed_time(t1) / n
+    assert ops.read_status(status) == 0, "device status set in the mixed step"
+    return {"ms_per_step": mixed_ms, "graph_ms_per_step": graph_mixed_ms, "steps": n,
+            "separate_ms_per_step": eager_ms, "separate_graph_ms_per_step": graph_ms,
+            "bitwise_equal_to_separate": same,
+            "note": "store, then one msgl_attn_mixed call (decode ranges, extend behind them by "
+                    "programmatic dependent launch, decode merge)"}
 
 
 def measure_graph(args, step, stream, eager_ms, dev):

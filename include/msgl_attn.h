@@ -208,6 +208,59 @@ MSGL_API msgl_status msgl_attn_decode_append(const msgl_kv_pool *pool, const msg
                                     size_t workspace_bytes, uint32_t *status, msgl_stream_t stream);
 
 /*
+ * One batch of chunked-prefill rows or of decode rows, as the mixed step
+ * below takes them.  Each field has the meaning, layout and ownership of
+ * the msgl_attn_extend / msgl_attn_decode argument of the same name.  An
+ * empty batch (num_reqs = 0) is allowed and launches nothing.
+ */
+typedef struct msgl_extend_batch {
+    msgl_page_table pages;
+    const void *q;                 /* device bf16 [total_tokens, num_q_heads, head_dim] */
+    const int32_t *prefix_lens;    /* device int32 [num_reqs] */
+    const int32_t *ext_lens;       /* device int32 [num_reqs] */
+    const int32_t *cu_ext;         /* device int32 [num_reqs + 1] */
+    const int32_t *positions;      /* device int32 [total_tokens] or NULL */
+    int32_t num_reqs, total_tokens, max_ext_len, max_seq_len;
+    void *o;                       /* device bf16 [total_tokens, num_q_heads, head_dim] (output) */
+    float *lse;                    /* device fp32 [total_tokens, num_q_heads] (output) */
+} msgl_extend_batch;
+
+typedef struct msgl_decode_batch {
+    msgl_page_table pages;
+    const void *q;                 /* device bf16 [num_reqs, num_q_heads, head_dim] */
+    const int32_t *seq_lens;       /* device int32 [num_reqs] */
+    int32_t num_reqs, max_seq_len;
+    void *o;                       /* device bf16 [num_reqs, num_q_heads, head_dim] (output) */
+    float *lse;                    /* device fp32 [num_reqs, num_q_heads] (output) */
+} msgl_decode_batch;
+
+/*
+ * Mixed step: the chunked-prefill batch and the decode batch of one forward
+ * in a single call.  Under chunked prefill a forward carries prefill chunks
+ * and decode rows together ("Mini-SGLang 实战指南", §6.1 "Chunked
+ * Prefill"), and the engine works to keep the GPU from idling between the
+ * pieces of a step (§6.6 "Overlap Scheduling").  The results are those of
+ * msgl_attn_extend(ext) and msgl_attn_decode(dec) on the same inputs, bit
+ * for bit; only the schedule differs.  The decode's key-range kernel runs
+ * first; the extend is launched behind it with programmatic dependent
+ * launch, so its CTAs take each SM as soon as that SM's decode range is
+ * done instead of waiting for the slowest range; the decode's LSE merge
+ * runs last.  Every launch shape depends on host scalars only, so the call
+ * can be captured in a CUDA graph.
+ *
+ *   workspace   device scratch of at least
+ *               msgl_decode_workspace_size(dec->num_reqs, ...) +
+ *               msgl_extend_workspace_size(...) bytes, 256-byte aligned
+ *               (NULL when that total is 0); fully rewritten by every call
+ * Host validation and device status bits are those of the two calls.  On a
+ * validation failure of either batch nothing is launched.
+ */
+MSGL_API msgl_status msgl_attn_mixed(const msgl_kv_pool *pool, const msgl_extend_batch *ext,
+                                     const msgl_decode_batch *dec, int32_t num_q_heads, float scale,
+                                     void *workspace, size_t workspace_bytes, uint32_t *status,
+                                     msgl_stream_t stream);
+
+/*
  * Decode for callers that cannot allocate device memory.  It has no
  * counterpart on the pages describing the engine: it is msgl_attn_decode
  * with its split scratch taken from a fixed array inside the library
@@ -223,10 +276,16 @@ MSGL_API msgl_status msgl_attn_decode_append(const msgl_kv_pool *pool, const msg
  * msgl_decode_workspace_size() exceeds that size returns
  * MSGL_ERR_WORKSPACE (msgl_last_error() gives both sizes) without launching.
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call before capturing any stream.  All calls on a device share the
- * array, which keeps the last call's contents (no call relies on them);
- * calls whose kernels overlap on the GPU race on it, so order them.
+ * (cudaGetSymbolAddress, with that device current) and caches it.  Under
+ * CUDA's lazy module loading that first call is also what loads the module
+ * and places the 32 MiB on the device, an implicit allocation with its
+ * possible synchronisation: make it once at start-up, before capturing any
+ * stream and outside latency-critical loops.  The cached address assumes
+ * one CUDA context per device for the life of the process; after a device
+ * reset, or under a different driver-API context, use a fresh process.
+ * All calls on a device share the array, which keeps the last call's
+ * contents (no call relies on them); calls whose kernels overlap on the GPU
+ * race on it, so order them.
  */
 #define MSGL_DECODE_NOALLOC_SCRATCH_BYTES (32u << 20)
 

@@ -88,14 +88,29 @@ msgl_status check_scale(float scale) {
 namespace msgl {
 // Lets other translation units of the library set this thread's error text.
 void set_last_error(const char *msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+
+int sm_count() {
+    static int cached[64];   // per device; racing first calls store the same value
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int sms = (dev >= 0 && dev < 64) ? cached[dev] : 0;
+    if (sms == 0) {
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 1;
+        if (dev >= 0 && dev < 64) cached[dev] = sms;
+    }
+    return sms;
+}
 }  // namespace msgl
 
-static msgl_status decode_impl(const msgl_kv_pool *pool, const msgl_page_table *pages, const void *q,
-                               int32_t num_q_heads, const void *k_new, const void *v_new,
-                               const int32_t *new_loc, const int32_t *seq_lens, int32_t num_reqs,
-                               int32_t max_seq_len, float scale, void *o, float *lse, void *workspace,
-                               size_t workspace_bytes, uint32_t *status, msgl_stream_t stream) {
-    g_last_error[0] = 0;
+// Validates a decode call and fills its kernel arguments.  `ws_offset` bytes of the
+// workspace are reserved for other use (the mixed step puts nothing there today).
+static msgl_status prepare_decode(const msgl_kv_pool *pool, const msgl_page_table *pages, const void *q,
+                                  int32_t num_q_heads, const void *k_new, const void *v_new,
+                                  const int32_t *new_loc, const int32_t *seq_lens, int32_t num_reqs,
+                                  int32_t max_seq_len, float scale, void *o, float *lse, void *workspace,
+                                  size_t workspace_bytes, uint32_t *status, msgl::DecodeArgs &a,
+                                  msgl::DecodePlan &plan) {
     msgl::PoolView pv;
     msgl::PageView pg;
     msgl_status s = check_pool(pool, pv);
@@ -103,23 +118,23 @@ static msgl_status decode_impl(const msgl_kv_pool *pool, const msgl_page_table *
     if ((s = check_heads(num_q_heads, pool->num_kv_heads))) return s;
     if ((s = check_scale(scale))) return s;
     if (num_reqs < 0) return fail(MSGL_ERR_INVALID_ARG, "num_reqs < 0");
+    a = msgl::DecodeArgs{};
+    a.num_reqs = num_reqs;
     if (num_reqs == 0) return MSGL_OK;
     if ((s = check_pages(pages, num_reqs, pg))) return s;
     if (max_seq_len <= 0) return fail(MSGL_ERR_INVALID_ARG, "max_seq_len must be > 0");
     if (!q || !seq_lens || !o || !lse) return fail(MSGL_ERR_INVALID_ARG, "q, seq_lens, o and lse must be non-NULL");
     if (!aligned16(q) || !aligned16(o)) return fail(MSGL_ERR_INVALID_ARG, "q and o must be 16-byte aligned");
-    const msgl::DecodePlan plan = msgl::plan_decode(num_reqs, num_q_heads, pool->num_kv_heads, max_seq_len);
+    plan = msgl::plan_decode(num_reqs, num_q_heads, pool->num_kv_heads, max_seq_len);
     if (!workspace || workspace_bytes < plan.workspace)
         return fail(MSGL_ERR_WORKSPACE, "decode needs %zu workspace bytes, got %zu", plan.workspace,
                     workspace ? workspace_bytes : (size_t)0);
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return fail(MSGL_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-    msgl::DecodeArgs a{};
     a.pool = pv;
     a.pages = pg;
     a.q = static_cast<const __nv_bfloat16 *>(q);
     a.seq_lens = seq_lens;
-    a.num_reqs = num_reqs;
     a.hq = num_q_heads;
     a.max_seq_len = max_seq_len;
     a.scale = scale;
@@ -131,10 +146,70 @@ static msgl_status decode_impl(const msgl_kv_pool *pool, const msgl_page_table *
     a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
     a.v_new = static_cast<const __nv_bfloat16 *>(v_new);
     a.new_loc = new_loc;
+    return MSGL_OK;
+}
+
+static msgl_status decode_impl(const msgl_kv_pool *pool, const msgl_page_table *pages, const void *q,
+                               int32_t num_q_heads, const void *k_new, const void *v_new,
+                               const int32_t *new_loc, const int32_t *seq_lens, int32_t num_reqs,
+                               int32_t max_seq_len, float scale, void *o, float *lse, void *workspace,
+                               size_t workspace_bytes, uint32_t *status, msgl_stream_t stream) {
+    g_last_error[0] = 0;
+    msgl::DecodeArgs a;
+    msgl::DecodePlan plan{};
+    msgl_status s = prepare_decode(pool, pages, q, num_q_heads, k_new, v_new, new_loc, seq_lens, num_reqs,
+                                   max_seq_len, scale, o, lse, workspace, workspace_bytes, status, a, plan);
+    if (s || num_reqs == 0) return s;
     cudaError_t e = msgl::launch_decode(a, plan, (cudaStream_t)stream);
     return e == cudaSuccess ? MSGL_OK : cuda_fail(e, "decode launch");
 }
 
+// Validates an extend call and fills its kernel arguments (a.num_reqs = 0: nothing to launch).
+static msgl_status prepare_extend(const msgl_kv_pool *pool, const msgl_page_table *pages, const void *q,
+                                  int32_t num_q_heads, const int32_t *prefix_lens, const int32_t *ext_lens,
+                                  const int32_t *cu_ext, const int32_t *positions, int32_t num_reqs,
+                                  int32_t total_tokens, int32_t max_ext_len, int32_t max_seq_len, float scale,
+                                  void *o, float *lse, void *workspace, size_t workspace_bytes,
+                                  uint32_t *status, msgl::ExtendArgs &a) {
+    msgl::PoolView pv;
+    msgl::PageView pg;
+    msgl_status s = check_pool(pool, pv);
+    if (s) return s;
+    if ((s = check_heads(num_q_heads, pool->num_kv_heads))) return s;
+    if ((s = check_scale(scale))) return s;
+    if (num_reqs < 0 || total_tokens < 0 || max_ext_len < 0 || max_seq_len < 0)
+        return fail(MSGL_ERR_INVALID_ARG, "negative size");
+    a = msgl::ExtendArgs{};
+    if (num_reqs == 0 || total_tokens == 0) return MSGL_OK;
+    if ((s = check_pages(pages, num_reqs, pg))) return s;
+    if (max_ext_len == 0 || max_seq_len < max_ext_len)
+        return fail(MSGL_ERR_INVALID_ARG, "need 0 < max_ext_len <= max_seq_len");
+    if (!q || !prefix_lens || !ext_lens || !cu_ext || !o || !lse)
+        return fail(MSGL_ERR_INVALID_ARG, "q, prefix_lens, ext_lens, cu_ext, o and lse must be non-NULL");
+    if (!aligned16(q) || !aligned16(o)) return fail(MSGL_ERR_INVALID_ARG, "q and o must be 16-byte aligned");
+    const size_t need = msgl::extend_workspace_bytes(num_reqs, total_tokens, num_q_heads,
+                                                     pool->num_kv_heads, max_seq_len);
+    if (need > 0 && (!workspace || workspace_bytes < need))
+        return fail(MSGL_ERR_WORKSPACE, "extend needs %zu workspace bytes", need);
+    a.pool = pv;
+    a.pages = pg;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.prefix_lens = prefix_lens;
+    a.ext_lens = ext_lens;
+    a.cu_ext = cu_ext;
+    a.positions = positions;
+    a.num_reqs = num_reqs;
+    a.total_tokens = total_tokens;
+    a.hq = num_q_heads;
+    a.max_ext_len = max_ext_len;
+    a.max_seq_len = max_seq_len;
+    a.scale = scale;
+    a.o = static_cast<__nv_bfloat16 *>(o);
+    a.lse = lse;
+    a.workspace = workspace;
+    a.status = status;
+    return MSGL_OK;
+}
 
 extern "C" {
 
@@ -224,45 +299,50 @@ msgl_status msgl_attn_extend(const msgl_kv_pool *pool, const msgl_page_table *pa
                              float *lse, void *workspace, size_t workspace_bytes,
                              uint32_t *status, msgl_stream_t stream) {
     g_last_error[0] = 0;
-    msgl::PoolView pv;
-    msgl::PageView pg;
-    msgl_status s = check_pool(pool, pv);
-    if (s) return s;
-    if ((s = check_heads(num_q_heads, pool->num_kv_heads))) return s;
-    if ((s = check_scale(scale))) return s;
-    if (num_reqs < 0 || total_tokens < 0 || max_ext_len < 0 || max_seq_len < 0)
-        return fail(MSGL_ERR_INVALID_ARG, "negative size");
-    if (num_reqs == 0 || total_tokens == 0) return MSGL_OK;
-    if ((s = check_pages(pages, num_reqs, pg))) return s;
-    if (max_ext_len == 0 || max_seq_len < max_ext_len)
-        return fail(MSGL_ERR_INVALID_ARG, "need 0 < max_ext_len <= max_seq_len");
-    if (!q || !prefix_lens || !ext_lens || !cu_ext || !o || !lse)
-        return fail(MSGL_ERR_INVALID_ARG, "q, prefix_lens, ext_lens, cu_ext, o and lse must be non-NULL");
-    if (!aligned16(q) || !aligned16(o)) return fail(MSGL_ERR_INVALID_ARG, "q and o must be 16-byte aligned");
-    const size_t need = msgl::extend_workspace_bytes(num_reqs, total_tokens, num_q_heads,
-                                                     pool->num_kv_heads, max_seq_len);
-    if (need > 0 && (!workspace || workspace_bytes < need))
-        return fail(MSGL_ERR_WORKSPACE, "extend needs %zu workspace bytes", need);
-    msgl::ExtendArgs a{};
-    a.pool = pv;
-    a.pages = pg;
-    a.q = static_cast<const __nv_bfloat16 *>(q);
-    a.prefix_lens = prefix_lens;
-    a.ext_lens = ext_lens;
-    a.cu_ext = cu_ext;
-    a.positions = positions;
-    a.num_reqs = num_reqs;
-    a.total_tokens = total_tokens;
-    a.hq = num_q_heads;
-    a.max_ext_len = max_ext_len;
-    a.max_seq_len = max_seq_len;
-    a.scale = scale;
-    a.o = static_cast<__nv_bfloat16 *>(o);
-    a.lse = lse;
-    a.workspace = workspace;
-    a.status = status;
+    msgl::ExtendArgs a;
+    msgl_status s = prepare_extend(pool, pages, q, num_q_heads, prefix_lens, ext_lens, cu_ext, positions,
+                                   num_reqs, total_tokens, max_ext_len, max_seq_len, scale, o, lse, workspace,
+                                   workspace_bytes, status, a);
+    if (s || a.num_reqs == 0) return s;
     cudaError_t e = msgl::launch_extend(a, (cudaStream_t)stream);
     return e == cudaSuccess ? MSGL_OK : cuda_fail(e, "extend launch");
+}
+
+msgl_status msgl_attn_mixed(const msgl_kv_pool *pool, const msgl_extend_batch *ext, const msgl_decode_batch *dec,
+                            int32_t num_q_heads, float scale, void *workspace, size_t workspace_bytes,
+                            uint32_t *status, msgl_stream_t stream) {
+    g_last_error[0] = 0;
+    if (!ext || !dec) return fail(MSGL_ERR_INVALID_ARG, "ext and dec must be non-NULL");
+    // the decode partials take the front of the workspace, the extend's share follows
+    msgl::DecodeArgs da;
+    msgl::DecodePlan plan{};
+    msgl_status s = prepare_decode(pool, &dec->pages, dec->q, num_q_heads, nullptr, nullptr, nullptr,
+                                   dec->seq_lens, dec->num_reqs, dec->max_seq_len, scale, dec->o, dec->lse,
+                                   workspace, workspace_bytes, status, da, plan);
+    if (s) return s;
+    const size_t dec_bytes = dec->num_reqs > 0 ? (plan.workspace + 255) / 256 * 256 : 0;
+    msgl::ExtendArgs ea;
+    void *ext_ws = workspace && workspace_bytes > dec_bytes ? static_cast<char *>(workspace) + dec_bytes : nullptr;
+    s = prepare_extend(pool, &ext->pages, ext->q, num_q_heads, ext->prefix_lens, ext->ext_lens, ext->cu_ext,
+                       ext->positions, ext->num_reqs, ext->total_tokens, ext->max_ext_len, ext->max_seq_len,
+                       scale, ext->o, ext->lse, ext_ws, ext_ws ? workspace_bytes - dec_bytes : 0, status, ea);
+    if (s) return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaSuccess;
+    if (da.num_reqs > 0 && ea.num_reqs > 0) {
+        // split first; the extend's CTAs fill SMs as the split's ranges finish; merge last
+        e = msgl::launch_decode(da, plan, st, msgl::DecodePhase::kSplit);
+        if (e == cudaSuccess) {
+            ea.pdl = true;
+            e = msgl::launch_extend(ea, st);
+        }
+        if (e == cudaSuccess) e = msgl::launch_decode(da, plan, st, msgl::DecodePhase::kMerge);
+    } else if (da.num_reqs > 0) {
+        e = msgl::launch_decode(da, plan, st);
+    } else if (ea.num_reqs > 0) {
+        e = msgl::launch_extend(ea, st);
+    }
+    return e == cudaSuccess ? MSGL_OK : cuda_fail(e, "mixed step launch");
 }
 
 msgl_status msgl_read_status(const uint32_t *status, uint32_t *flags, msgl_stream_t stream) {

@@ -735,15 +735,7 @@ Launch decode_launch_shape(int hkv, int slices, bool box) {
     int st = (int)((kSmemBudget - 1024 - 64) / (stage_bytes(L.hg, box) + sizeof(TileMeta) + 16));
     L.stages = st < 2 ? 2 : (st > kMaxStages ? kMaxStages : st);
     L.smem = decode_smem_bytes(L.hg, L.stages, box);
-    static int sm_count[64];   // per device, filled on first use (same value if two threads race)
-    int dev = 0;
-    cudaGetDevice(&dev);
-    int sms = (dev >= 0 && dev < 64) ? sm_count[dev] : 0;
-    if (sms == 0) {
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (sms <= 0) sms = 1;
-        if (dev >= 0 && dev < 64) sm_count[dev] = sms;
-    }
+    const int sms = sm_count();
     const int groups = hkv / L.hg;
     int ctas = sms / groups;
     if (ctas < 1) ctas = 1;
@@ -764,7 +756,7 @@ DecodePlan plan_decode(int32_t num_reqs, int32_t hq, int32_t hkv, int32_t max_se
     return p;
 }
 
-cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream, DecodePhase phase) {
     if (a.num_reqs == 0) return cudaSuccess;
     const int hkv = a.pool.hkv;
     const int slices = decode_slices(a.hq / hkv);
@@ -826,15 +818,17 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     k.new_loc = a.new_loc;
     (void)plan;
     if (L.smem > (size_t)kSmemBudget) return cudaErrorInvalidValue;
-    dim3 grid(L.ctas, hkv / L.hg);
-    if (box)
-        decode_split_kernel<true><<<grid, 32 * (L.hg * slices + 1), L.smem, stream>>>(km, vm, k);
-    else
-        decode_split_kernel<false><<<grid, 32 * (L.hg * slices + 1), L.smem, stream>>>(km, vm, k);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if (phase != DecodePhase::kMerge) {
+        dim3 grid(L.ctas, hkv / L.hg);
+        if (box)
+            decode_split_kernel<true><<<grid, 32 * (L.hg * slices + 1), L.smem, stream>>>(km, vm, k);
+        else
+            decode_split_kernel<false><<<grid, 32 * (L.hg * slices + 1), L.smem, stream>>>(km, vm, k);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess || phase == DecodePhase::kSplit) return e;
+    }
     // programmatic dependent launch: the merge's launch and its seq_lens scan overlap the
-    // tail of the split kernel
+    // tail of the kernel before it (the split, or the extend of a mixed step)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((a.hq + 7) / 8, a.num_reqs);
     cfg.blockDim = dim3(256);

@@ -73,6 +73,7 @@ struct ExtendKernelArgs {
     __nv_bfloat16 *o;
     float *lse;
     uint32_t *status;
+    int32_t pdl_wait;     // launched behind a kernel it must not outlive (see the kernel's start)
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_flag,
@@ -89,6 +90,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap vt_map, const ExtendKernelArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Launched with programmatic dependent launch behind the decode split of a mixed step,
+    // this grid may start before the split has finished.  The last CTA waits for it, so the
+    // grid cannot complete before the split has: whatever the stream runs next after this
+    // grid sees the split's partials.  It reads nothing the split writes.  The last CTA is
+    // handed out last, long after the split is done, so the wait returns at once.
+    if (a.pdl_wait && blockIdx.x == gridDim.x - 1 && threadIdx.x == 0)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // ---- work item: heaviest token blocks first, then kv head, then request
     const int per_rank = a.pool.hkv * a.num_reqs;
@@ -613,10 +621,24 @@ cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t stream) {
     k.o = a.o;
     k.lse = a.lse;
     k.status = a.status;
+    k.pdl_wait = a.pdl ? 1 : 0;
     const long long grid = (long long)k.nblk * hkv * a.num_reqs;
     if (grid >= INT_MAX) return cudaErrorInvalidValue;
-    extend_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(qm, km, vm, ktm, vtm, k);
-    return cudaGetLastError();
+    if (!a.pdl) {
+        extend_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(qm, km, vm, ktm, vtm, k);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, extend_tc_kernel, qm, km, vm, ktm, vtm, k);
 }
 
 }  // namespace msgl

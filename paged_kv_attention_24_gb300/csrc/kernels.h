@@ -39,7 +39,11 @@ struct DecodeArgs {
     const __nv_bfloat16 *k_new = nullptr, *v_new = nullptr;   // append mode (see msgl_attn_decode_append)
     const int32_t *new_loc = nullptr;
 };
-cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream);
+// Which kernels of a decode call to launch: the split (partials per key range), the
+// merge (LSE fold of the partials, launched with programmatic dependent launch), or both.
+enum class DecodePhase { kSplit, kMerge, kBoth };
+cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream,
+                          DecodePhase phase = DecodePhase::kBoth);
 
 // --------------------------------------------------------------- extend
 size_t extend_workspace_bytes(int32_t num_reqs, int32_t total_tokens, int32_t hq, int32_t hkv,
@@ -56,11 +60,18 @@ struct ExtendArgs {
     float *lse;
     void *workspace;
     uint32_t *status;
+    // launch with programmatic dependent launch: CTAs may start while the previous
+    // kernel on the stream still runs (every CTA waits for it before it exits)
+    bool pdl = false;
 };
 cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t stream);
 
 // cuTensorMapEncodeTiled from the driver (NULL if unavailable); looked up once.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
+// SM count of the current device, queried once per device and cached (0..63;
+// other ordinals are queried on every call).
+int sm_count();
 
 // Sets the text msgl_last_error() returns on this thread.
 void set_last_error(const char *msg);

@@ -47,6 +47,20 @@ class _Pages(ctypes.Structure):
                 ("width", ctypes.c_int32)]
 
 
+class _ExtendBatch(ctypes.Structure):
+    _fields_ = [("pages", _Pages), ("q", ctypes.c_void_p), ("prefix_lens", ctypes.c_void_p),
+                ("ext_lens", ctypes.c_void_p), ("cu_ext", ctypes.c_void_p), ("positions", ctypes.c_void_p),
+                ("num_reqs", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
+                ("max_ext_len", ctypes.c_int32), ("max_seq_len", ctypes.c_int32),
+                ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p)]
+
+
+class _DecodeBatch(ctypes.Structure):
+    _fields_ = [("pages", _Pages), ("q", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+                ("num_reqs", ctypes.c_int32), ("max_seq_len", ctypes.c_int32),
+                ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p)]
+
+
 _lib = None
 _lock = threading.Lock()
 
@@ -64,6 +78,8 @@ SIGNATURES = {
     "msgl_attn_decode": ([PP, PT, P, I32, P, I32, I32, F32, P, P, P, SZ, P, P], ctypes.c_int),
     "msgl_attn_decode_append": ([PP, PT, P, I32, P, P, P, P, I32, I32, F32, P, P, P, SZ, P, P], ctypes.c_int),
     "msgl_attn_decode_noalloc": ([PP, PT, P, I32, P, I32, I32, F32, P, P, P, P], ctypes.c_int),
+    "msgl_attn_mixed": ([PP, ctypes.POINTER(_ExtendBatch), ctypes.POINTER(_DecodeBatch), I32, F32, P, SZ, P, P],
+                        ctypes.c_int),
     "msgl_selftest_wait_timeout": ([P, I64, P], ctypes.c_int),
     "msgl_read_status": ([P, ctypes.POINTER(ctypes.c_uint32), P], ctypes.c_int),
     "msgl_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -258,6 +274,61 @@ def attn_decode_append(pool: KVPool, q: torch.Tensor, k_new: torch.Tensor, v_new
         _stream(stream))
     _check(rc, "msgl_attn_decode_append")
     return out, lse
+
+
+def attn_mixed(pool: KVPool, scale: float,
+               ext_q: torch.Tensor, ext_page_table: torch.Tensor, prefix_lens: torch.Tensor,
+               ext_lens: torch.Tensor, cu_ext: torch.Tensor, max_ext_len: int, max_ext_seq_len: int,
+               dec_q: torch.Tensor, dec_page_table: torch.Tensor, seq_lens: torch.Tensor, max_dec_seq_len: int,
+               positions: Optional[torch.Tensor] = None, ext_out=None, ext_lse=None, dec_out=None, dec_lse=None,
+               workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None, stream=None):
+    """The extend batch and the decode batch of one forward in one call (msgl_attn_mixed).
+
+    Same results as :func:`attn_extend` and :func:`attn_decode`; returns
+    ((o_ext, lse_ext), (o_dec, lse_dec)).
+    """
+    _need(ext_q, "ext_q", torch.bfloat16)
+    _need(dec_q, "dec_q", torch.bfloat16)
+    for name, t in (("prefix_lens", prefix_lens), ("ext_lens", ext_lens), ("cu_ext", cu_ext),
+                    ("seq_lens", seq_lens)):
+        _need(t, name, torch.int32)
+    if positions is not None:
+        _need(positions, "positions", torch.int32)
+    T, hq, d = ext_q.shape
+    B = int(dec_q.shape[0])
+    if dec_q.shape[1] != hq:
+        raise ValueError("ext_q and dec_q must have the same number of q heads")
+    ext_out = torch.empty_like(ext_q) if ext_out is None else ext_out
+    ext_lse = torch.empty(T, hq, dtype=torch.float32, device=ext_q.device) if ext_lse is None else ext_lse
+    dec_out = torch.empty_like(dec_q) if dec_out is None else dec_out
+    dec_lse = torch.empty(B, hq, dtype=torch.float32, device=dec_q.device) if dec_lse is None else dec_lse
+    for name, t, dt in (("ext_out", ext_out, torch.bfloat16), ("ext_lse", ext_lse, torch.float32),
+                        ("dec_out", dec_out, torch.bfloat16), ("dec_lse", dec_lse, torch.float32)):
+        _need(t, name, dt)
+    if workspace is None:
+        workspace = _workspace(mixed_workspace_size(B, T, int(prefix_lens.shape[0]), hq, pool.num_kv_heads,
+                                                    max_ext_seq_len, max_dec_seq_len, d), dec_q.device)
+    eb = _ExtendBatch(_pages(ext_page_table), ext_q.data_ptr(), prefix_lens.data_ptr(), ext_lens.data_ptr(),
+                      cu_ext.data_ptr(), None if positions is None else positions.data_ptr(),
+                      int(prefix_lens.shape[0]), T, int(max_ext_len), int(max_ext_seq_len),
+                      ext_out.data_ptr(), ext_lse.data_ptr())
+    db = _DecodeBatch(_pages(dec_page_table), dec_q.data_ptr(), seq_lens.data_ptr(), B, int(max_dec_seq_len),
+                      dec_out.data_ptr(), dec_lse.data_ptr())
+    pc = pool.c()
+    rc = load().msgl_attn_mixed(ctypes.byref(pc), ctypes.byref(eb), ctypes.byref(db), hq, float(scale),
+                                _ptr(workspace),
+                                0 if workspace is None else workspace.numel() * workspace.element_size(),
+                                _ptr(status), _stream(stream))
+    _check(rc, "msgl_attn_mixed")
+    return (ext_out, ext_lse), (dec_out, dec_lse)
+
+
+def mixed_workspace_size(dec_reqs: int, ext_tokens: int, ext_reqs: int, hq: int, hkv: int,
+                         max_ext_seq_len: int, max_dec_seq_len: int, head_dim: int = 128) -> int:
+    """Workspace bytes of :func:`attn_mixed`: the decode's (rounded up to 256) plus the extend's."""
+    dec = decode_workspace_size(dec_reqs, hq, hkv, max_dec_seq_len, head_dim) if dec_reqs > 0 else 0
+    ext = extend_workspace_size(ext_reqs, ext_tokens, hq, hkv, max_ext_seq_len, head_dim) if ext_reqs > 0 else 0
+    return (dec + 255) // 256 * 256 + ext
 
 
 NOALLOC_SCRATCH_BYTES = 32 << 20
