@@ -16,7 +16,11 @@
 // exits.  Host code cannot use the array's name as a device address (on the
 // host it names a stand-in object), so the first call on each device looks
 // up the real address with cudaGetSymbolAddress while that device is
-// current, and caches it.
+// current, and caches it.  Under lazy module loading that lookup is also
+// what loads the module and places the array on the device, so callers make
+// their first call at start-up.  The cache is keyed by device ordinal: it
+// assumes one context per device for the life of the process (a device
+// reset or another driver-API context needs a fresh process).
 //
 // All calls on a device share the one array and it keeps whatever the last
 // call left in it.  Nothing has to start at zero: every partial the merge

@@ -99,3 +99,21 @@ def test_workspace_size_queries(lib):
     assert lib.msgl_decode_workspace_size(4, 16, 8, 64, 200) == 0   # unsupported head_dim
     assert lib.msgl_decode_workspace_size(0, 16, 8, 128, 200) == 0
     assert big % 256 == 0
+
+
+def test_noalloc_scratch_size_agrees_with_binding(lib):
+    """The Python copy of the built-in scratch size equals the header's macro and the size
+    the library itself reports when it refuses an over-size batch (a host-side check made
+    before any CUDA call)."""
+    from paged_kv_attention_24_gb300 import ops
+    text = open(os.path.join(ROOT, "include", "msgl_attn.h")).read()
+    m = re.search(r"#define MSGL_DECODE_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", text)
+    assert m and int(m.group(1)) << int(m.group(2)) == ops.NOALLOC_SCRATCH_BYTES
+    pool = ops._Pool(16, 16, 4096, 64, 8, 128)
+    pages = ops._Pages(16, 64, 64)
+    rc = lib.msgl_attn_decode_noalloc(ctypes.byref(pool), ctypes.byref(pages), 16, 64, 16, 600, 4096, 0.1,
+                                      16, 16, None, None)
+    assert rc == 6
+    need = lib.msgl_decode_workspace_size(600, 64, 8, 128, 4096)
+    msg = lib.msgl_last_error().decode()
+    assert f"needs {need} scratch bytes" in msg and f"holds {ops.NOALLOC_SCRATCH_BYTES}" in msg, msg
