@@ -103,8 +103,7 @@ int sm_count() {
 }
 }  // namespace msgl
 
-// Validates a decode call and fills its kernel arguments.  `ws_offset` bytes of the
-// workspace are reserved for other use (the mixed step puts nothing there today).
+// Validates a decode call and fills its kernel arguments (a.num_reqs = 0: nothing to launch).
 static msgl_status prepare_decode(const msgl_kv_pool *pool, const msgl_page_table *pages, const void *q,
                                   int32_t num_q_heads, const void *k_new, const void *v_new,
                                   const int32_t *new_loc, const int32_t *seq_lens, int32_t num_reqs,
