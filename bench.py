@@ -52,6 +52,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--no-append", action="store_true", help="skip the fused append+decode timing")
+    ap.add_argument("--seed", type=int, default=None,
+                    help="workload seed (default 1000 + config id; rank r adds 7 r)")
+    ap.add_argument("--nvtx", action="store_true",
+                    help="mark store / extend / decode of every step with NVTX ranges (for a profiler timeline)")
     ap.add_argument("--no-mixed", action="store_true", help="skip the mixed-step (msgl_attn_mixed) timing")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-config legs (configs 2, 3 and 4) after the headline step")
@@ -271,7 +275,7 @@ def run_reference(args):
     from paged_kv_attention_24_gb300 import workloads as W
     from paged_kv_attention_24_gb300 import accounting as A
     import oracle
-    w = W.config(args.config, device="cpu", page_size=args.page_size)
+    w = W.config(args.config, device="cpu", seed=args.seed, page_size=args.page_size)
     threads = oracle.default_threads()
     per_step = max(1.0, 90.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
@@ -321,7 +325,8 @@ def run_ours(args):
     from paged_kv_attention_24_gb300 import workloads as W
     from paged_kv_attention_24_gb300 import accounting as A
 
-    w = W.config(args.config, device=dev, seed=1000 + args.config + 7 * rank, page_size=args.page_size)
+    base_seed = 1000 + args.config if args.seed is None else args.seed
+    w = W.config(args.config, device=dev, seed=base_seed + 7 * rank, page_size=args.page_size)
     pool = ops.KVPool(w.k_pool, w.v_pool, w.page_size)
     k_new, v_new, loc = w.new_tokens()
     e, d = w.extend, w.decode
@@ -341,21 +346,33 @@ def run_ours(args):
     launches_per_step = (1 if loc.numel() else 0) + (1 if e is not None else 0) + \
         ((2 if ws_d is not None else 1) if d is not None else 0)
 
+    nvtx = torch.cuda.nvtx if args.nvtx else None
+
+    def mark(name):
+        if nvtx:
+            nvtx.range_pop() if name is None else nvtx.range_push(name)
+
     def step(ev=None):
         if ev:
             ev[0].record(stream)
+        mark("msgl_store_kv")
         ops.store_kv(pool, k_new, v_new, loc, status=status)
+        mark(None)
         if ev:
             ev[1].record(stream)
         if e is not None:
+            mark("msgl_attn_extend")
             ops.attn_extend(pool, e.q, e.page_table, e.prefix_lens, e.ext_lens, e.cu_ext,
                             e.max_ext_len, e.max_seq_len, w.scale, positions=e.positions,
                             out=o_e, lse=l_e, workspace=ws_e, status=status)
+            mark(None)
         if ev:
             ev[2].record(stream)
         if d is not None:
+            mark("msgl_attn_decode")
             ops.attn_decode(pool, d.q, d.page_table, d.seq_lens, d.max_seq_len, w.scale,
                             out=o_d, lse=l_d, workspace=ws_d, status=status)
+            mark(None)
         if ev:
             ev[3].record(stream)
 
