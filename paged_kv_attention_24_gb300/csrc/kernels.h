@@ -61,7 +61,8 @@ struct ExtendArgs {
     void *workspace;
     uint32_t *status;
     // launch with programmatic dependent launch: CTAs may start while the previous
-    // kernel on the stream still runs (every CTA waits for it before it exits)
+    // kernel on the stream still runs (the grid's last CTA waits for that kernel, so the
+    // grid does not complete before it)
     bool pdl = false;
 };
 cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t stream);
