@@ -117,3 +117,36 @@ def test_noalloc_scratch_size_agrees_with_binding(lib):
     need = lib.msgl_decode_workspace_size(600, 64, 8, 128, 4096)
     msg = lib.msgl_last_error().decode()
     assert f"needs {need} scratch bytes" in msg and f"holds {ops.NOALLOC_SCRATCH_BYTES}" in msg, msg
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    """The binding's ctypes structures have the C structs' sizes and field offsets
+    (a C program built against include/msgl_attn.h prints them)."""
+    import subprocess
+    from paged_kv_attention_24_gb300 import ops
+    src = tmp_path / "layout.c"
+    structs = {"msgl_kv_pool": (ops._Pool, ["k_pool", "v_pool", "num_slots", "page_size", "num_kv_heads",
+                                            "head_dim"]),
+               "msgl_page_table": (ops._Pages, ["page_ids", "stride", "width"]),
+               "msgl_extend_batch": (ops._ExtendBatch, ["pages", "q", "prefix_lens", "ext_lens", "cu_ext",
+                                                        "positions", "num_reqs", "total_tokens", "max_ext_len",
+                                                        "max_seq_len", "o", "lse"]),
+               "msgl_decode_batch": (ops._DecodeBatch, ["pages", "q", "seq_lens", "num_reqs", "max_seq_len",
+                                                        "o", "lse"])}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "msgl_attn.h"', "int main(void) {"]
+    for name, (_, fields) in structs.items():
+        lines.append(f'printf("{name} size %zu\\n", sizeof({name}));')
+        for f in fields:
+            lines.append(f'printf("{name} {f} %zu\\n", offsetof({name}, {f}));')
+    lines += ["return 0;", "}"]
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = {}
+    for line in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.splitlines():
+        name, field, value = line.split()
+        got[(name, field)] = int(value)
+    for name, (cls, fields) in structs.items():
+        assert got[(name, "size")] == ctypes.sizeof(cls), name
+        for f in fields:
+            assert got[(name, f)] == getattr(cls, f).offset, (name, f)
