@@ -181,6 +181,83 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+class NvmlClockPoller:
+    """SM clock and clock-event reasons read through NVML every millisecond while the timed
+    region runs (nvidia-smi's loop cannot sample inside a region of a few milliseconds).
+    Read-only queries; returns None when NVML cannot be loaded."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    SM_CLOCK = 1   # NVML_CLOCK_SM
+
+    def __init__(self, device_index: int, period_s: float = 0.001):
+        import ctypes
+        import threading
+        self.samples, self.max_mhz, self.period = [], None, period_s
+        self.stop_flag = threading.Event()
+        self.thread = None
+        self.lib = self.dev = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            dev = ctypes.c_void_p()
+            ok = False
+            try:
+                import torch
+                uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+                for u in (uuid, "GPU-" + uuid):
+                    if lib.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(dev)) == 0:
+                        ok = True
+                        break
+            except Exception:
+                ok = False
+            if not ok and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(device_index), ctypes.byref(dev)) != 0:
+                return
+            mx = ctypes.c_uint(0)
+            if lib.nvmlDeviceGetMaxClockInfo(dev, self.SM_CLOCK, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self.reason_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.lib, self.dev = lib, dev
+        except (OSError, AttributeError):
+            self.lib = None
+
+    def _run(self):
+        import ctypes
+        import time as _t
+        clk, rs = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        while not self.stop_flag.is_set():
+            if self.lib.nvmlDeviceGetClockInfo(self.dev, self.SM_CLOCK, ctypes.byref(clk)) == 0:
+                r = rs.value if self.reason_fn(self.dev, ctypes.byref(rs)) == 0 else 0
+                self.samples.append((clk.value, r))
+            _t.sleep(self.period)
+
+    def __enter__(self):
+        import threading
+        if self.lib is not None:
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.thread is not None:
+            self.stop_flag.set()
+            self.thread.join(timeout=2)
+        return False
+
+    def summary(self):
+        if self.lib is None or not self.samples:
+            return None
+        mhz = [m for m, _ in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        return {"sm_mhz_median": statistics.median(mhz), "sm_mhz_min": min(mhz), "sm_mhz_max": max(mhz),
+                "sm_max_mhz": self.max_mhz, "samples": len(mhz), "period_ms": self.period * 1e3,
+                "reasons": sorted(n for b, n in self.REASONS.items() if bits & b)}
+
+
 def dist_info():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -386,13 +463,14 @@ def run_ours(args):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for i in range(args.steps):
-            step(evs[i])
-        t_end.record(stream)
-        torch.cuda.synchronize()
+        with NvmlClockPoller(dev.index) as fine:
+            t_start = torch.cuda.Event(enable_timing=True)
+            t_end = torch.cuda.Event(enable_timing=True)
+            t_start.record(stream)
+            for i in range(args.steps):
+                step(evs[i])
+            t_end.record(stream)
+            torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
     total_ms = t_start.elapsed_time(t_end)
@@ -513,6 +591,7 @@ def run_ours(args):
         "mixed": mixed,
         "configs": extra,
         "clocks": clocks,
+        "clocks_in_region": fine.summary(),
     }
     print(json.dumps(line), flush=True)
     if ws > 1:
