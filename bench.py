@@ -560,6 +560,9 @@ def run_ours(args):
         extra = measure_other_configs(args, dev, peaks)
 
     if rank != 0:
+        if ws > 1:
+            torch.distributed.barrier()
+            torch.distributed.destroy_process_group()
         return 0
     clocks = clk.summary()
     line = {
@@ -595,6 +598,7 @@ def run_ours(args):
     }
     print(json.dumps(line), flush=True)
     if ws > 1:
+        torch.distributed.barrier()
         torch.distributed.destroy_process_group()
     return 0
 
