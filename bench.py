@@ -213,6 +213,7 @@ class NvmlClockPoller:
             except Exception:
                 ok = False
             if not ok and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(device_index), ctypes.byref(dev)) != 0:
+                lib.nvmlShutdown()
                 return
             mx = ctypes.c_uint(0)
             if lib.nvmlDeviceGetMaxClockInfo(dev, self.SM_CLOCK, ctypes.byref(mx)) == 0:
@@ -244,6 +245,8 @@ class NvmlClockPoller:
         if self.thread is not None:
             self.stop_flag.set()
             self.thread.join(timeout=2)
+        if self.lib is not None:
+            self.lib.nvmlShutdown()
         return False
 
     def summary(self):
