@@ -306,59 +306,81 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_o = ptx::umma_idesc_bf16(128, 128, false, true);
             bool ok = wait_or_abort(bar(kQFull), 0, abort_flag, a.status);
             ptx::tc_fence_after();
-            // S_t = Q_t K_j^T for tile t (8 MMAs over the 128 dims)
-            auto issue_s = [&](int t, int j) {
-                const uint32_t kb = sbase + kOffK + (j & 1) * kTile;
-                const uint32_t qb = sbase + kOffQ + t * kTile;
+            // The issuing thread runs at the tensor pipe's pace (an MMA issues once the one
+            // before it is nearly done), so every cycle it spends between two groups is a
+            // cycle the pipe idles.  Each group therefore tests, after its 4th MMA and with the
+            // non-blocking test_wait, the barrier the next group needs: the test's latency
+            // hides behind the MMAs still queued, and the bounded wait runs only when the
+            // phase has not completed yet.  Descriptors are built once and advanced by adding
+            // the offset (address >> 4) to their start-address field.
+            const uint64_t qdesc = ptx::umma_desc_sw128(sbase + kOffQ, 16, 1024);
+            const uint64_t kdesc = ptx::umma_desc_sw128(sbase + kOffK, 16, 1024);
+            const uint64_t vdesc = ptx::umma_desc_sw128(sbase + kOffV, kHalf, 1024);
+            // S_t = Q_t K_j^T for tile t (8 MMAs over the 128 dims); returns the test of
+            // (pb, pp), or false when pb is 0
+            auto issue_s = [&](int t, int j, uint32_t pb, uint32_t pp) -> bool {
+                const uint64_t qd = qdesc + (uint64_t)(t * (kTile >> 4));
+                const uint64_t kd = kdesc + (uint64_t)((j & 1) * (kTile >> 4));
+                bool r = false;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    ptx::tc_mma_ss(tmem + 128 * t, ptx::umma_desc_sw128(qb + off, 16, 1024),
-                                   ptx::umma_desc_sw128(kb + off, 16, 1024), idesc_s, kk > 0);
+                    const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                    ptx::tc_mma_ss(tmem + 128 * t, qd + off, kd + off, idesc_s, kk > 0);
+                    if (kk == 3 && pb) r = ptx::mbar_test_wait(pb, pp);
                 }
                 ptx::tc_commit(bar(kSFull + t));
+                return r;
             };
             // O_t += P_t V_j (P from TMEM, 8 MMAs over the 128 keys)
-            auto issue_pv = [&](int t, int j) {
-                const uint32_t vb = sbase + kOffV + (j % kVStages) * kTile;
+            auto issue_pv = [&](int t, int j, uint32_t pb, uint32_t pp) -> bool {
+                const uint64_t vd = vdesc + (uint64_t)((j % kVStages) * (kTile >> 4));
+                bool r = false;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    ptx::tc_mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8,
-                                   ptx::umma_desc_sw128(vb + kk * 2048, kHalf, 1024), idesc_o,
-                                   (j > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < 8; ++kk) {
+                    ptx::tc_mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8, vd + (uint64_t)(kk * (2048 >> 4)),
+                                   idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                    if (kk == 3 && pb) r = ptx::mbar_test_wait(pb, pp);
+                }
                 ptx::tc_commit(bar(kOFull + t));
+                return r;
             };
             // Order per K/V tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).  The next S of a
             // tile goes in right after its PV (same TMEM columns; tcgen05 MMAs from one
             // thread execute in order), so tile 0's next softmax overlaps tile 1's.
+            bool v_ok = false, p0_ok = false;   // PV_0(j)'s barriers, tested during S_1(j)
             if (ok && (ok = wait_or_abort(bar(kKFull + 0), 0, abort_flag, a.status))) {
                 ptx::tc_fence_after();
-                if (nkv0 > 0) issue_s(0, 0);
-                if (nkv1 > 0) issue_s(1, 0);
+                if (nkv0 > 0) issue_s(0, 0, 0, 0);
+                if (nkv1 > 0) v_ok = issue_s(1, 0, bar(kVFull + 0), 0);
                 ptx::tc_commit(bar(kKEmpty + 0));
             }
             for (int j = 0; ok && j < nkv; ++j) {
                 const int jn = j + 1, sn = jn & 1, phn = (jn >> 1) & 1;
-                if (!(ok = wait_or_abort(bar(kVFull + j % kVStages), (j / kVStages) & 1, abort_flag, a.status))) break;
-                ptx::tc_fence_after();
-                if (j < nkv0) {
-                    if (!(ok = wait_or_abort(bar(kPFull + 0), j & 1, abort_flag, a.status))) break;
-                    ptx::tc_fence_after();
-                    issue_pv(0, j);
-                }
                 const bool more = jn < nkv;
-                if (more) {
-                    if (!(ok = wait_or_abort(bar(kKFull + sn), phn, abort_flag, a.status))) break;
+                if (!v_ok && !(ok = wait_or_abort(bar(kVFull + j % kVStages), (j / kVStages) & 1, abort_flag, a.status)))
+                    break;
+                bool k_ok = false, p1_ok = false;
+                if (j < nkv0) {
+                    if (!p0_ok && !(ok = wait_or_abort(bar(kPFull + 0), j & 1, abort_flag, a.status))) break;
                     ptx::tc_fence_after();
-                    if (jn < nkv0) issue_s(0, jn);
+                    k_ok = issue_pv(0, j, more ? bar(kKFull + sn) : 0u, phn);
+                }
+                if (more) {
+                    if (!k_ok && !(ok = wait_or_abort(bar(kKFull + sn), phn, abort_flag, a.status))) break;
+                    ptx::tc_fence_after();
+                    if (jn < nkv0) p1_ok = issue_s(0, jn, j < nkv1 ? bar(kPFull + 1) : 0u, j & 1);
                 }
                 if (j < nkv1) {
-                    if (!(ok = wait_or_abort(bar(kPFull + 1), j & 1, abort_flag, a.status))) break;
+                    if (!p1_ok && !(ok = wait_or_abort(bar(kPFull + 1), j & 1, abort_flag, a.status))) break;
                     ptx::tc_fence_after();
-                    issue_pv(1, j);
+                    issue_pv(1, j, 0, 0);
                 }
+                v_ok = p0_ok = false;
                 if (more) {
-                    if (jn < nkv1) issue_s(1, jn);
+                    if (jn < nkv1) {
+                        v_ok = issue_s(1, jn, bar(kVFull + jn % kVStages), (jn / kVStages) & 1);
+                        if (jn < nkv0) p0_ok = ptx::mbar_test_wait(bar(kPFull + 0), jn & 1);
+                    }
                     ptx::tc_commit(bar(kKEmpty + sn));
                 }
                 ptx::tc_commit(bar(kVEmpty + j % kVStages));
