@@ -341,13 +341,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
                     if (kk == 3 && pb) r = ptx::mbar_test_wait(pb, pp);
                 }
-                ptx::tc_commit(bar(kOFull + t));
+                // only the epilogue waits for O_t: the completion of S_t(j+1), issued after
+                // PV_t(j) by this thread, already tells the softmax that PV_t(j) is done
+                if (j == (t ? nkv1 : nkv0) - 1) ptx::tc_commit(bar(kOFull + t));
                 return r;
             };
             // Order per K/V tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).  The next S of a
             // tile goes in right after its PV (same TMEM columns; tcgen05 MMAs from one
             // thread execute in order), so tile 0's next softmax overlaps tile 1's.
-            bool v_ok = false, p0_ok = false;   // PV_0(j)'s barriers, tested during S_1(j)
+            bool v_ok = false;   // V_j's barrier, tested during S_1(j)
             if (ok && (ok = wait_or_abort(bar(kKFull + 0), 0, abort_flag, a.status))) {
                 ptx::tc_fence_after();
                 if (nkv0 > 0) issue_s(0, 0, 0, 0);
@@ -361,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 bool k_ok = false, p1_ok = false;
                 if (j < nkv0) {
-                    if (!p0_ok && !(ok = wait_or_abort(bar(kPFull + 0), j & 1, abort_flag, a.status))) break;
+                    if (!(ok = wait_or_abort(bar(kPFull + 0), j & 1, abort_flag, a.status))) break;
                     ptx::tc_fence_after();
                     k_ok = issue_pv(0, j, more ? bar(kKFull + sn) : 0u, phn);
                 }
@@ -375,12 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tc_fence_after();
                     issue_pv(1, j, 0, 0);
                 }
-                v_ok = p0_ok = false;
+                v_ok = false;
                 if (more) {
-                    if (jn < nkv1) {
-                        v_ok = issue_s(1, jn, bar(kVFull + jn % kVStages), (jn / kVStages) & 1);
-                        if (jn < nkv0) p0_ok = ptx::mbar_test_wait(bar(kPFull + 0), jn & 1);
-                    }
+                    if (jn < nkv1) v_ok = issue_s(1, jn, bar(kVFull + jn % kVStages), (jn / kVStages) & 1);
                     ptx::tc_commit(bar(kKEmpty + sn));
                 }
                 ptx::tc_commit(bar(kVEmpty + j % kVStages));
@@ -407,8 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int my_nkv = t ? nkv1 : nkv0;
         bool ok = true;
         for (int j = 0; j < my_nkv; ++j) {
+            // S_t(j) complete: PV_t(j-1), issued before it by the same thread, is done too
             if (!(ok = wait_or_abort(bar(kSFull + t), j & 1, abort_flag, a.status))) break;
-            if (j > 0 && !(ok = wait_or_abort(bar(kOFull + t), (j - 1) & 1, abort_flag, a.status))) break;
             ptx::tc_fence_after();
             const bool masked = j >= jm;             // uniform: only tiles past the first row's limit
             const int lim = limit - j * kKeys;       // key c of this tile is visible iff c <= lim
@@ -481,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) ptx::mbar_arrive(bar(kPFull + t));
         }
         // epilogue: O / l -> bf16, lse = ln(sum exp(s))
-        if (ok && my_nkv > 0 && wait_or_abort(bar(kOFull + t), (my_nkv - 1) & 1, abort_flag, a.status)) {
+        if (ok && my_nkv > 0 && wait_or_abort(bar(kOFull + t), 0, abort_flag, a.status)) {
             ptx::tc_fence_after();
             const int tok_g = tok0 + t * R + tok_l;
             const bool store = row_valid && tok_g < a.total_tokens;
