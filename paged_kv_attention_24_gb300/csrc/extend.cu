@@ -423,18 +423,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 128; ++i)
                     if (i > lim) v[i] = __float_as_uint(-INFINITY);
             }
-            // row max in four independent 3-input chains (16 deep each)
-            float mxa = -INFINITY, mxb = -INFINITY, mxc = -INFINITY, mxd = -INFINITY;
+            // row max in four independent 3-input chains (16 deep each), scaled to log2 units
+            auto row_max = [&]() -> float {
+                float mxa = -INFINITY, mxb = -INFINITY, mxc = -INFINITY, mxd = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < 128; i += 8) {
-                mxa = ptx::max3(mxa, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-                mxb = ptx::max3(mxb, __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
-                mxc = ptx::max3(mxc, __uint_as_float(v[i + 4]), __uint_as_float(v[i + 5]));
-                mxd = ptx::max3(mxd, __uint_as_float(v[i + 6]), __uint_as_float(v[i + 7]));
-            }
-            const float m_new = fmaxf(m_ref, fmaxf(fmaxf(mxa, mxb), fmaxf(mxc, mxd)) * a.scale_log2);
-            const bool need = m_new > m_ref + 8.f;
-            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                for (int i = 0; i < 128; i += 8) {
+                    mxa = ptx::max3(mxa, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                    mxb = ptx::max3(mxb, __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                    mxc = ptx::max3(mxc, __uint_as_float(v[i + 4]), __uint_as_float(v[i + 5]));
+                    mxd = ptx::max3(mxd, __uint_as_float(v[i + 6]), __uint_as_float(v[i + 7]));
+                }
+                return fmaxf(fmaxf(mxa, mxb), fmaxf(mxc, mxd)) * a.scale_log2;
+            };
+            // The first tile sets the reference m_ref to the row max.  Later tiles write P from
+            // the reference straight away: a score more than 2^8 above it makes some p > 256
+            // and so the row sum >= 256 (a NaN fails the test too).  Only then is the row max
+            // taken; a row whose max passes m_ref + 8 moves its reference there, its O and l
+            // are rescaled, and P is written again.  Every p stays below 2^8 either way.
+            if (j == 0) m_ref = fmaxf(m_ref, row_max());
+            float ls = 0.f;
+#pragma unroll 1
+            for (int pass = 0;; ++pass) {
+                // P = 2^(s * scale_log2 - m_ref) (masked scores are -inf -> 0), back over S as bf16
+                const uint64_t sc2 = ptx::f2_pack(a.scale_log2, a.scale_log2);
+                const uint64_t nm2 = ptx::f2_pack(-m_ref, -m_ref);
+                uint64_t l2 = ptx::f2_pack(0.f, 0.f);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int e = 32 * c + 2 * i;
+                        const uint64_t x2 = ptx::f2_fma(ptx::f2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                                        sc2, nm2);
+                        float x0, x1;
+                        ptx::f2_unpack(x2, x0, x1);
+                        const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+                        l2 = ptx::f2_add(l2, ptx::f2_pack(p0, p1));
+                        pk[i] = ptx::pack_bf16(p0, p1);
+                    }
+                    ptx::tc_st16(tS + 16 * c, pk);
+                }
+                float la, lb;
+                ptx::f2_unpack(l2, la, lb);
+                ls = la + lb;
+                if (pass == 1 || j == 0 || __all_sync(0xffffffffu, ls < 256.f)) break;
+                const float m_new = fmaxf(m_ref, row_max());
+                const bool need = m_new > m_ref + 8.f;
+                if (!__any_sync(0xffffffffu, need)) break;
                 const float alpha = need ? ptx::ex2(m_ref - m_new) : 1.f;
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
@@ -447,33 +483,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ptx::tc_wait_st();
                 l *= alpha;
+                if (need) m_ref = m_new;
             }
-            if (need) m_ref = m_new;
-            // P = 2^(s * scale_log2 - m_ref) (masked scores are -inf -> 0), back over S as bf16
-            const uint64_t sc2 = ptx::f2_pack(a.scale_log2, a.scale_log2);
-            const uint64_t nm2 = ptx::f2_pack(-m_ref, -m_ref);
-            uint64_t l2 = ptx::f2_pack(0.f, 0.f);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int e = 32 * c + 2 * i;
-                    const uint64_t x2 = ptx::f2_fma(ptx::f2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
-                                                    sc2, nm2);
-                    float x0, x1;
-                    ptx::f2_unpack(x2, x0, x1);
-                    const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
-                    l2 = ptx::f2_add(l2, ptx::f2_pack(p0, p1));
-                    pk[i] = ptx::pack_bf16(p0, p1);
-                }
-                ptx::tc_st16(tS + 16 * c, pk);
-            }
-            {
-                float la, lb;
-                ptx::f2_unpack(l2, la, lb);
-                l += la + lb;
-            }
+            l += ls;
             ptx::tc_wait_st();
             ptx::tc_fence_before();
             __syncwarp();
