@@ -354,7 +354,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_fence_after();
                 if (nkv0 > 0) issue_s(0, 0, 0, 0);
                 if (nkv1 > 0) v_ok = issue_s(1, 0, bar(kVFull + 0), 0);
-                ptx::tc_commit(bar(kKEmpty + 0));
             }
             for (int j = 0; ok && j < nkv; ++j) {
                 const int jn = j + 1, sn = jn & 1, phn = (jn >> 1) & 1;
@@ -378,11 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     issue_pv(1, j, 0, 0);
                 }
                 v_ok = false;
-                if (more) {
-                    if (jn < nkv1) v_ok = issue_s(1, jn, bar(kVFull + jn % kVStages), (jn / kVStages) & 1);
-                    ptx::tc_commit(bar(kKEmpty + sn));
-                }
-                ptx::tc_commit(bar(kVEmpty + j % kVStages));
+                if (more && jn < nkv1) v_ok = issue_s(1, jn, bar(kVFull + jn % kVStages), (jn / kVStages) & 1);
             }
             // drain: every MMA issued above has completed once this fires
             ptx::tc_commit(bar(kDrain));
@@ -405,10 +400,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_ref = -INFINITY, l = 0.f;
         const int my_nkv = t ? nkv1 : nkv0;
         bool ok = true;
+        // The K/V stages are released from here, not by commits of the MMA thread (whose
+        // every instruction between two MMA groups leaves the tensor pipe idle): the
+        // completion of S_r(j), r the last tile (it has the most K/V tiles), means every
+        // MMA issued before it is done, so K_j (read by S_0(j) and S_r(j)) and V_{j-1} (read
+        // by PV_0(j-1) and PV_r(j-1)) are free.
+        const bool releaser = lane == 0 && warp == (nB > 0 ? 8 : 4);
         for (int j = 0; j < my_nkv; ++j) {
             // S_t(j) complete: PV_t(j-1), issued before it by the same thread, is done too
             if (!(ok = wait_or_abort(bar(kSFull + t), j & 1, abort_flag, a.status))) break;
             ptx::tc_fence_after();
+            if (releaser) {
+                ptx::mbar_arrive(bar(kKEmpty + (j & 1)));
+                if (j > 0) ptx::mbar_arrive(bar(kVEmpty + (j - 1) % kVStages));
+            }
             const bool masked = j >= jm;             // uniform: only tiles past the first row's limit
             const int lim = limit - j * kKeys;       // key c of this tile is visible iff c <= lim
             // one TMEM read of the row's 128 scores
