@@ -316,11 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t qdesc = ptx::umma_desc_sw128(sbase + kOffQ, 16, 1024);
             const uint64_t kdesc = ptx::umma_desc_sw128(sbase + kOffK, 16, 1024);
             const uint64_t vdesc = ptx::umma_desc_sw128(sbase + kOffV, kHalf, 1024);
-            // S_t = Q_t K_j^T for tile t (8 MMAs over the 128 dims); returns the test of
-            // (pb, pp), or false when pb is 0
-            auto issue_s = [&](int t, int j, uint32_t pb, uint32_t pp) -> bool {
+            // S_t = Q_t K^T for tile t from the K stage at descriptor kd (8 MMAs over the 128
+            // dims); returns the test of (pb, pp), or false when pb is 0
+            auto s_group = [&](int t, uint64_t kd, uint32_t pb, uint32_t pp) -> bool {
                 const uint64_t qd = qdesc + (uint64_t)(t * (kTile >> 4));
-                const uint64_t kd = kdesc + (uint64_t)((j & 1) * (kTile >> 4));
                 bool r = false;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
@@ -331,16 +330,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_commit(bar(kSFull + t));
                 return r;
             };
-            // O_t += P_t V_j (P from TMEM, 8 MMAs over the 128 keys)
-            auto issue_pv = [&](int t, int j, uint32_t pb, uint32_t pp) -> bool {
-                const uint64_t vd = vdesc + (uint64_t)((j % kVStages) * (kTile >> 4));
+            // O_t += P_t V from the V stage at descriptor vd (P from TMEM, 8 MMAs over the 128
+            // keys); acc = 0 starts O_t
+            auto pv_group = [&](int t, uint64_t vd, bool acc, uint32_t pb, uint32_t pp) -> bool {
                 bool r = false;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     ptx::tc_mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8, vd + (uint64_t)(kk * (2048 >> 4)),
-                                   idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                                   idesc_o, (acc || kk > 0) ? 1u : 0u);
                     if (kk == 3 && pb) r = ptx::mbar_test_wait(pb, pp);
                 }
+                return r;
+            };
+            auto issue_s = [&](int t, int j, uint32_t pb, uint32_t pp) -> bool {
+                return s_group(t, kdesc + (uint64_t)((j & 1) * (kTile >> 4)), pb, pp);
+            };
+            auto issue_pv = [&](int t, int j, uint32_t pb, uint32_t pp) -> bool {
+                const bool r = pv_group(t, vdesc + (uint64_t)((j % kVStages) * (kTile >> 4)), j > 0, pb, pp);
                 // only the epilogue waits for O_t: the completion of S_t(j+1), issued after
                 // PV_t(j) by this thread, already tells the softmax that PV_t(j) is done
                 if (j == (t ? nkv1 : nkv0) - 1) ptx::tc_commit(bar(kOFull + t));
@@ -355,7 +361,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (nkv0 > 0) issue_s(0, 0, 0, 0);
                 if (nkv1 > 0) v_ok = issue_s(1, 0, bar(kVFull + 0), 0);
             }
-            for (int j = 0; ok && j < nkv; ++j) {
+            int j = 0;
+            {
+                // Steady state: both tiles have K/V tiles j and j + 1, so all four groups run
+                // and none is a tile's last; the stages advance by counters.
+                const int jss = nB > 0 ? nkv0 - 1 : 0;
+                uint32_t vs = 0, vpar = 0;   // V stage of tile j and the parity of its phase
+                uint32_t ks = 1, kpar = 0;   // K stage of tile j + 1 and the parity of its phase
+                for (; ok && j < jss; ++j) {
+                    if (!v_ok && !(ok = wait_or_abort(bar(kVFull) + 8u * vs, vpar, abort_flag, a.status))) break;
+                    if (!(ok = wait_or_abort(bar(kPFull + 0), j & 1, abort_flag, a.status))) break;
+                    ptx::tc_fence_after();
+                    const uint64_t vd = vdesc + (uint64_t)(vs * (kTile >> 4));
+                    const uint32_t b_k = bar(kKFull) + 8u * ks;
+                    if (!pv_group(0, vd, j > 0, b_k, kpar) && !(ok = wait_or_abort(b_k, kpar, abort_flag, a.status)))
+                        break;
+                    ptx::tc_fence_after();
+                    const uint64_t kd = kdesc + (uint64_t)(ks * (kTile >> 4));
+                    if (!s_group(0, kd, bar(kPFull + 1), j & 1) &&
+                        !(ok = wait_or_abort(bar(kPFull + 1), j & 1, abort_flag, a.status)))
+                        break;
+                    ptx::tc_fence_after();
+                    pv_group(1, vd, j > 0, 0, 0);
+                    vs = vs == kVStages - 1 ? 0 : vs + 1;
+                    vpar ^= vs == 0 ? 1u : 0u;
+                    v_ok = s_group(1, kd, bar(kVFull) + 8u * vs, vpar);
+                    ks ^= 1u;
+                    kpar ^= ks == 0 ? 1u : 0u;
+                }
+            }
+            for (; ok && j < nkv; ++j) {
                 const int jn = j + 1, sn = jn & 1, phn = (jn >> 1) & 1;
                 const bool more = jn < nkv;
                 if (!v_ok && !(ok = wait_or_abort(bar(kVFull + j % kVStages), (j / kVStages) & 1, abort_flag, a.status)))
