@@ -15,7 +15,8 @@
 // * A CTA owns two such tiles (2R tokens) of one request and one kv head and
 //   streams 128-key K and V tiles through 2-stage (K) and 3-stage (V) rings.
 //   At page_size >= 16 a page that is a contiguous, fully valid run of pool
-//   rows arrives in one tiled TMA box per 64-dim half, and any other keys
+//   rows arrives in tiled TMA boxes (K: one per 64-dim half; V: one per 32
+//   keys, both halves, into V's 16-key block layout), and any other keys
 //   are gathered four pool rows per copy (TMA gather4).  Below 16 every key
 //   is its own run, and 16-byte cp.async copies replace the gathers (a TMA
 //   instruction per four 128-byte rows cannot keep up).  A key beyond the
@@ -30,7 +31,16 @@
 //   warps 4-7 and 8-11 run the online softmax of tile 0 and tile 1 (one
 //   TMEM lane = one row per thread).  While one warpgroup exponentiates,
 //   the tensor core works on the other tile.  O is rescaled lazily: only
-//   when a row's running max grows by more than 2^8 (so P stays <= 256).
+//   when a row's running max grows by more than 2^8 (so P stays <= 256);
+//   after the first K/V tile the row max is taken only when a row sum
+//   shows that some score may have grown that much.
+// * The issuing thread runs at the tensor pipe's pace and shares its SM
+//   sub-partition with two softmax warps, so every instruction it executes
+//   between MMA groups idles the pipe: it tests the next group's barrier
+//   while the current group is queued, releases no K/V stage itself (the
+//   last tile's softmax warp does, on seeing S complete), commits O only
+//   after a tile's last PV, and runs a steady-state loop without per-tile
+//   conditions.
 // * Every mbarrier wait is bounded; a timeout sets MSGL_DEVERR_TIMEOUT and
 //   the CTA winds down after its copies and MMAs have landed.
 #include <cuda.h>
@@ -53,6 +63,12 @@ constexpr int kVStages = 3;                // V tiles in flight (V is needed lat
 constexpr int kThreads = 384;              // 12 warps
 constexpr uint32_t kHalf = 16384;          // 128 rows x 128 bytes (64 bf16)
 constexpr uint32_t kTile = 2 * kHalf;      // 128 x 128 bf16
+// With tiled page copies (page size >= 16), V tiles are stored as 8 blocks of 16 keys,
+// each block [half][16 keys][128 B], so that one copy brings both 64-dim halves of up to
+// 32 keys and every PV MMA (16 keys) reads one block, its halves kVHalf bytes apart.  At
+// 16 keys per page the copy engine's per-copy cost bounds the loads, and this halves the
+// V copies.  The 16-byte-copy path (smaller pages) lays V out as K.
+constexpr uint32_t kVBlock = 4096, kVHalf = 2048;
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + 2 * kTile;
 constexpr uint32_t kOffV = kOffK + kStages * kTile;
@@ -69,6 +85,7 @@ struct ExtendKernelArgs {
     const int32_t *prefix_lens, *ext_lens, *cu_ext, *positions;
     int32_t hq, group, rows_per_tile, q_box_rows, total_tokens, num_reqs, nblk, oob_row;
     int32_t box_rows;     // rows of one tiled pool box (min(page_size, 128)); 0 = gather only
+    int32_t v_blocks;     // V tiles in blocks of 16 keys (tiled page copies); 0 = laid out as K
     float scale_log2;
     __nv_bfloat16 *o;
     float *lse;
@@ -278,15 +295,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t parity = is_v ? ((j / kVStages) & 1) ^ 1 : ((j >> 1) & 1) ^ 1;
                 if (!wait_or_abort(empty, parity, abort_flag, a.status)) break;
                 const uint32_t full = is_v ? bar(kVFull + sv) : bar(kKFull + (j & 1));
-                const uint32_t dst = (is_v ? sbase + kOffV + sv * kTile : sbase + kOffK + (j & 1) * kTile) + lane * 512;
+                // this lane's four keys: rows 4 lane .. 4 lane + 3 (K), or their place in V's blocks
+                const bool vb = is_v && a.v_blocks;
+                const uint32_t dst = vb ? sbase + kOffV + sv * kTile + (uint32_t)(lane >> 2) * kVBlock +
+                                              (uint32_t)(lane & 3) * 512u
+                                        : (is_v ? sbase + kOffV + sv * kTile : sbase + kOffK + (j & 1) * kTile) +
+                                              lane * 512;
+                const uint32_t half_off = vb ? kVHalf : kHalf;
                 if (lane == 0) ptx::mbar_arrive_expect_tx(full, kTile);
                 __syncwarp();
                 if (!tiled) {
                     ptx::tma_gather4(dst, gm, 0, rows[0], rows[1], rows[2], rows[3], full);
-                    ptx::tma_gather4(dst + kHalf, gm, 64, rows[0], rows[1], rows[2], rows[3], full);
+                    ptx::tma_gather4(dst + half_off, gm, 64, rows[0], rows[1], rows[2], rows[3], full);
                 } else if (lane == box_lead) {
-                    ptx::tma_load_3d(dst, tm, 0, g, (int)slot0, full);
-                    ptx::tma_load_3d(dst + kHalf, tm, 64, g, (int)slot0, full);
+                    if (vb) {
+                        // the page's blocks, two (8 KB) at most per copy: {64 dims, head g, 16
+                        // slots, 2 halves, 1 or 2 blocks}.  Larger copies held up the K copies
+                        // queued behind them on the same copy engine.
+                        for (int n = 0; n < (BR > 32 ? BR / 32 : 1); ++n)
+                            ptx::tma_load_5d(dst + (uint32_t)n * 2u * kVBlock, tm, 0, g, (int)slot0 + 32 * n, 0, 0,
+                                             full);
+                    } else {
+                        ptx::tma_load_3d(dst, tm, 0, g, (int)slot0, full);
+                        ptx::tma_load_3d(dst + kHalf, tm, 64, g, (int)slot0, full);
+                    }
                 }
                 issued = j + 1;
             }
@@ -315,7 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the offset (address >> 4) to their start-address field.
             const uint64_t qdesc = ptx::umma_desc_sw128(sbase + kOffQ, 16, 1024);
             const uint64_t kdesc = ptx::umma_desc_sw128(sbase + kOffK, 16, 1024);
-            const uint64_t vdesc = ptx::umma_desc_sw128(sbase + kOffV, kHalf, 1024);
+            const uint64_t vdesc = ptx::umma_desc_sw128(sbase + kOffV, a.v_blocks ? kVHalf : kHalf, 1024);
+            const uint32_t vstep = (a.v_blocks ? kVBlock : 16u * 128u) >> 4;   // MMA kk's 16 keys
             // S_t = Q_t K^T for tile t from the K stage at descriptor kd (8 MMAs over the 128
             // dims); returns the test of (pb, pp), or false when pb is 0
             auto s_group = [&](int t, uint64_t kd, uint32_t pb, uint32_t pp) -> bool {
@@ -336,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool r = false;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    ptx::tc_mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8, vd + (uint64_t)(kk * (2048 >> 4)),
+                    ptx::tc_mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8, vd + (uint64_t)(kk * vstep),
                                    idesc_o, (acc || kk > 0) ? 1u : 0u);
                     if (kk == 3 && pb) r = ptx::mbar_test_wait(pb, pp);
                 }
@@ -654,16 +687,35 @@ cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t stream) {
     memset(&vtm, 0, sizeof vtm);
     const int page = 1 << a.pool.log2_ps;
     const int box_rows = page >= 16 ? (page < kKeys ? page : kKeys) : 0;
-    for (int which = 0; box_rows > 0 && which < 2; ++which) {
+    const int v_blocks = box_rows > 0;
+    if (box_rows > 0) {
         cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv, (cuuint64_t)a.pool.num_slots};
         cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)hkv * kHeadDim * 2};
         cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
         cuuint32_t es[3] = {1, 1, 1};
-        if (enc(which ? &vtm : &ktm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                (void *)(which ? a.pool.v : a.pool.k), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+        if (enc(&ktm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void *)a.pool.k, dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
+        if (v_blocks) {
+            // V: 5D view {64 dims, Hkv heads, 16 slots, 2 halves (128 bytes apart), blocks of
+            // 16 slots}: one box brings one or two blocks in V's layout.  The view aliases slots
+            // across its 3rd and 5th dimensions, so its bounds do not guard the pool: the
+            // kernel uses a box only for a page whose slots are all valid.
+            cuuint64_t vdims[5] = {64, (cuuint64_t)hkv, (cuuint64_t)a.pool.num_slots, 2, (cuuint64_t)(kKeys / 16)};
+            cuuint64_t vstrides[4] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)hkv * kHeadDim * 2, 128,
+                                      (cuuint64_t)16 * hkv * kHeadDim * 2};
+            cuuint32_t vbox[5] = {64, 1, 16, 2, (cuuint32_t)(box_rows > 32 ? 2 : box_rows / 16)};
+            cuuint32_t ves[5] = {1, 1, 1, 1, 1};
+            if (enc(&vtm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, (void *)a.pool.v, vdims, vstrides, vbox, ves,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return cudaErrorInvalidValue;
+        } else if (enc(&vtm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void *)a.pool.v, dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+            return cudaErrorInvalidValue;
+        }
     }
     static bool attr_set[64];
     int dev = 0;
@@ -690,6 +742,7 @@ cudaError_t launch_extend(const ExtendArgs &a, cudaStream_t stream) {
     k.nblk = (a.max_ext_len + 2 * R - 1) / (2 * R);
     k.oob_row = (int)pool_rows;
     k.box_rows = box_rows;
+    k.v_blocks = v_blocks;
     k.scale_log2 = a.scale * kLog2e;
     k.o = a.o;
     k.lse = a.lse;
