@@ -178,11 +178,12 @@ def test_extend_long_prefix_many_tiles():
     assert_lse_close(lse, ref_l)
 
 
-@pytest.mark.parametrize("ps", [1, 4, 16])
+@pytest.mark.parametrize("ps", [1, 4, 16, 32, 64])
 def test_extend_bad_page_zeroes_affected_rows(ps):
     """A page id past the pool: status bit set; rows that would read it are zero, earlier rows exact.
 
-    Page sizes below 16 take the cp.async copy path, 16 the TMA path."""
+    Page sizes below 16 take the cp.async copy path, 16 and up the TMA path; at 16 and 32
+    the key tile holds whole pages copied as boxes and the bad page's rows gathered."""
     w = W.make_workload("badpage", 16, 8, 128, ps, seed=51, extend_prefix_lens=[64], extend_ext_lens=[100],
                         device="cuda")
     e = w.extend
