@@ -15,11 +15,11 @@
 // * A CTA owns two such tiles (2R tokens) of one request and one kv head and
 //   streams 128-key K and V tiles through 2-stage (K) and 3-stage (V) rings.
 //   At page_size >= 16 a page that is a contiguous, fully valid run of pool
-//   rows arrives in tiled TMA boxes (K: one per 64-dim half; V: one per 32
-//   keys, both halves, into V's 16-key block layout), and any other keys
-//   are gathered four pool rows per copy (TMA gather4).  Below 16 every key
-//   is its own run, and 16-byte cp.async copies replace the gathers (a TMA
-//   instruction per four 128-byte rows cannot keep up).  A key beyond the
+//   rows arrives in tiled TMA boxes (K: one per 64-dim half; V: both halves
+//   of 16 or 32 keys per box, into V's 16-key block layout), and any other
+//   keys are gathered four pool rows per copy (TMA gather4).  Below 16 every
+//   key is its own run, and 16-byte cp.async copies replace the gathers (a
+//   TMA instruction per four 128-byte rows cannot keep up).  A key beyond the
 //   causal range, or behind a bad page id, reads as zeros.
 // * tcgen05.mma (M = N = 128, K = 16 per instruction, bf16 in, fp32 out):
 //   S_t = Q_t K^T lands in TMEM (columns 0-127 for tile 0, 128-255 for tile
