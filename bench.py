@@ -79,7 +79,7 @@ def load_peaks():
 
 
 def tensor_peak(peaks, region_ms):
-    """The bf16 peak a tensor-bound kernel is judged against, by the length of the timed region.
+    """The bf16 peak a tensor-bound kernel is compared with, by the length of the timed region.
 
     A region of a few seconds or more runs under the power cap (sustained figure);
     a shorter one times the kernel in near-isolation (burst figure).
